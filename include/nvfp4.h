@@ -1,0 +1,223 @@
+/*
+ * nvfp4.h -- C ABI of libnvfp4.so: the NVFP4 (E2M1 codes + E4M3 scale per 16
+ * elements + FP32 per-tensor scale) W4A4 linear and MLP hot path on one
+ * Blackwell GPU (sm_103a).
+ *
+ * Sources, by page title and section:
+ *  - "PERFORMANCE -- verified hot-path audit and prioritized fixes"
+ *    (nvfp4-megamoe-kernel PERFORMANCE_AUDIT.md): P0 (activation global
+ *    scale amax/(6*448) computed on the device and handed to the kernel as a
+ *    (1,) device tensor, never read back by the host), P8 items 1-2
+ *    (quantization fused into the producer: RMSNorm + quantize), DOCTRINE 1
+ *    (no host state on the hot path).
+ *  - "CUDA: NVFP4 prefill on Blackwell leaves ~1.45x performance on the
+ *    table. Comparison + PoC" (llama.cpp discussion 28514), "What the patch
+ *    does": GLU output quantized straight into the next GEMM's activation
+ *    format, gate/up sharing one quantized input, batched-row rms_norm,
+ *    TMA + mbarrier fed FP4 MMA tiles; and its ncu finding that a 36-byte
+ *    interleaved FP4 block is only 4-byte aligned -- codes and scales are
+ *    therefore kept in separate, 16-byte aligned arrays here.
+ *  - "tp>1 prefill is host-bound: per-token fp4 GEMM + per-layer H2D
+ *    activation staging" (vllm.cpp issue 2144), "Fix directions" 1-3: one
+ *    launch set per T-token batch with a grid that scales with T,
+ *    activations resident on the device, quantization on the device.
+ *
+ * Conventions (all functions):
+ *  - Every pointer argument is a DEVICE pointer unless stated otherwise, owned
+ *    by the caller.  No function allocates, frees or synchronises; all work is
+ *    enqueued on `stream` (a cudaStream_t; NULL is the legacy default stream).
+ *  - The return value is a status (NVFP4_OK = 0).  Argument errors are
+ *    detected on the host before anything is enqueued.  NVFP4_ERR_CUDA
+ *    reports a launch error (cudaGetLastError); asynchronous failures show
+ *    up in the stream as usual.
+ *  - bf16 tensors are row-major with a row pitch given in ELEMENTS; bf16
+ *    base pointers and pitches must be 16-byte aligned (pitch % 8 == 0).
+ *  - A quantized tensor (nvfp4_tensor_t) of logical shape [rows x cols]:
+ *      codes: byte (r, k/2) at codes + r*ld + k/2 holds element k in its low
+ *             nibble when k is even, in its high nibble when k is odd; each
+ *             nibble is an E2M1 code (bit 3 sign, magnitudes 0, .5, 1, 1.5,
+ *             2, 3, 4, 6).  cols % 64 == 0; ld % 16 == 0; codes 16-B aligned.
+ *      sf:    one unsigned E4M3 scale per 16 consecutive elements of a row,
+ *             in 512-byte tiles of 128 rows x 4 scales: rows padded to a
+ *             multiple of 128, scale columns (cols/16) padded to a multiple of
+ *             4, tiles row-tile-major, and inside a tile the scale of row r,
+ *             column c at (r%32)*16 + (r%128)/32*4 + c%4.  Size:
+ *             nvfp4_sf_bytes(rows, cols); 128-B aligned; padding bytes are 0.
+ *      g:     fp32[1] per-tensor global scale (> 0).
+ *    Element value = E2M1(code) * E4M3(scale) * g.
+ */
+#ifndef NVFP4_H
+#define NVFP4_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* nvfp4_stream_t; /* identical to cudaStream_t */
+
+enum nvfp4_status {
+    NVFP4_OK = 0,
+    NVFP4_ERR_INVALID_ARG = 1, /* NULL pointer, bad shape (rows < 1, cols % 64 != 0, ...) */
+    NVFP4_ERR_MISALIGNED = 2,  /* pointer or pitch not aligned as documented */
+    NVFP4_ERR_UNSUPPORTED = 3, /* device is not compute capability 10.3 (sm_103a) */
+    NVFP4_ERR_CUDA = 4,        /* a CUDA runtime/driver call failed */
+    NVFP4_ERR_WORKSPACE = 5,   /* workspace missing or smaller than required */
+    NVFP4_ERR_TIMEOUT = 6      /* device-side: a pipeline wait exceeded its time limit */
+};
+
+/* Intermediate (SwiGLU output) global-scale modes of the fused gate/up GEMM. */
+enum nvfp4_inter_mode {
+    /* g_inter is an input: a scale fixed ahead of time (e.g. by one DYNAMIC
+     * warm-up call), used by the GEMM epilogue to requantize SwiGLU output
+     * straight into FP4 ("keep the warm-up scale as a device tensor"). */
+    NVFP4_INTER_STATIC = 0,
+    /* g_inter is an output: the epilogue stores bf16 SwiGLU output and its
+     * amax, then the scale max(amax,1e-8)/2688 is written to *g_inter on the
+     * device and the SwiGLU output is quantized with it (exact per-call
+     * scale, two extra HBM passes over T x I bf16). */
+    NVFP4_INTER_DYNAMIC = 1
+};
+
+/* A quantized matrix; see the conventions above. */
+typedef struct {
+    const uint8_t* codes;
+    const uint8_t* sf;
+    const float* g;
+    int64_t rows;
+    int64_t cols;
+    int64_t ld; /* bytes */
+} nvfp4_tensor_t;
+
+/* ------------------------------------------------------------ host helpers */
+
+/* Bytes of a codes array with ld = cols/2: rows * cols / 2. */
+size_t nvfp4_codes_bytes(int64_t rows, int64_t cols);
+/* Bytes of a scale array: pad128(rows) * pad4(cols/16). */
+size_t nvfp4_sf_bytes(int64_t rows, int64_t cols);
+/* Workspace of nvfp4_amax_scale (8 bytes, 256-B aligned). */
+size_t nvfp4_amax_workspace_bytes(void);
+/* Workspace of nvfp4_gemm_swiglu for an A of T rows and an intermediate of I
+ * columns: 256 bytes (STATIC) or 256 + T*I*2 bytes (DYNAMIC). */
+size_t nvfp4_swiglu_workspace_bytes(int64_t T, int64_t I, int inter_mode);
+/* Workspace of nvfp4_mlp (T tokens, hidden H, intermediate I). */
+size_t nvfp4_mlp_workspace_bytes(int64_t T, int64_t H, int64_t I, int inter_mode);
+/* Static description of a status code. */
+const char* nvfp4_status_string(int status);
+/* Reads (and if clear != 0 resets) the library's device-side status word of
+ * the current device, which kernels set when a pipeline wait times out.
+ * SYNCHRONOUS (a device-to-host copy); diagnostics and tests only. */
+int nvfp4_device_status(int* status_out, int clear);
+
+/* ------------------------------------------------------------- the path */
+
+/*
+ * nvfp4_amax_scale -- device per-tensor global scale.
+ *   g_out[0] = max(amax, 1e-8) / (6 * 448)  (binary32 division),
+ *   amax = max |v| over the bf16 matrix v.
+ * Source: "PERFORMANCE -- verified hot-path audit and prioritized fixes", P0
+ * (the runtime scale, computed on the device instead of via .item()).
+ *   x        bf16 [rows x cols], row pitch ldx elements.
+ *   norm_w   NULL, or bf16 [cols]: then v is the RMSNorm of x,
+ *            v = bf16(x * r * w), r = 1/sqrt(mean(x^2) + eps) per row
+ *            (the batched-row RMSNorm prologue).
+ *   g_out    fp32[1], written.
+ *   workspace >= nvfp4_amax_workspace_bytes(), 256-B aligned.  It must be
+ *            zero-filled ONCE after allocation; every call returns it to zero.
+ *            Calls sharing one workspace must be stream-ordered.
+ * Requires rows >= 1, cols >= 8, cols % 8 == 0.
+ */
+int nvfp4_amax_scale(const void* x, int64_t rows, int64_t cols, int64_t ldx,
+                     const void* norm_w, float eps, float* g_out,
+                     void* workspace, size_t workspace_bytes, nvfp4_stream_t stream);
+
+/*
+ * nvfp4_quantize -- bf16 -> NVFP4 with the device global scale g.
+ * Per 16-element block (binary32, one rounding per step):
+ *   s = E4M3_rne_satfinite( amax16 / (6*g) ),
+ *   code_i = s == 0 ? +0 : E2M1_rne_satfinite( v_i / (E4M3(s) * g) ).
+ * Sources: "PERFORMANCE -- verified hot-path audit and prioritized fixes",
+ * P0 and P8 item 2 (rmsnorm_quantize); "CUDA: NVFP4 prefill on Blackwell
+ * leaves ~1.45x performance on the table", item 2 (batched-row rms_norm).
+ *   x, ldx, norm_w, eps  as nvfp4_amax_scale (norm_w != NULL: quantize the
+ *            RMSNorm of x, computed exactly as nvfp4_amax_scale computes it).
+ *   g        fp32[1] device global scale.
+ *   codes    [rows][ld_codes] bytes, ld_codes >= cols/2, % 16 == 0.
+ *   sf       nvfp4_sf_bytes(rows, cols) bytes, 128-B aligned; padding written 0.
+ *   y_out    NULL, or bf16 [rows x cols] (pitch cols): receives v (export for
+ *            tests of the norm prologue).
+ * Requires rows >= 1, cols % 64 == 0.
+ */
+int nvfp4_quantize(const void* x, int64_t rows, int64_t cols, int64_t ldx,
+                   const void* norm_w, float eps, const float* g,
+                   uint8_t* codes, int64_t ld_codes, uint8_t* sf, void* y_out,
+                   nvfp4_stream_t stream);
+
+/*
+ * nvfp4_gemm -- block-scaled GEMM on the tensor cores (tcgen05
+ * kind::mxf4nvf4, fp32 accumulation in tensor memory):
+ *   out[m][n] = bf16( alpha * sum_k A[m,k] W[n,k] ),  alpha = fp32(gA * gW),
+ *   or, with residual != NULL, bf16( residual[m][n] + that bf16 ).
+ * Source: "CUDA: NVFP4 prefill on Blackwell leaves ~1.45x performance on the
+ * table" item 3 (TMA + mbarrier fed FP4 MMA accumulated in place);
+ * "tp>1 prefill is host-bound" fix direction 1 (one launch for all T rows).
+ *   A        activations, rows M = T (any M >= 1), cols K.
+ *   W        weights [N x K] (K-major, as nn.Linear stores them).
+ *   out      bf16 [M x N], pitch ldo; may alias residual (same pitch).
+ * Requires K == A->cols == W->cols, K % 64 == 0, N % 16 == 0.
+ */
+int nvfp4_gemm(const nvfp4_tensor_t* A, const nvfp4_tensor_t* W,
+               void* out, int64_t ldo, const void* residual, int64_t ldr,
+               nvfp4_stream_t stream);
+
+/*
+ * nvfp4_gemm_swiglu -- fused gate/up GEMM with SwiGLU epilogue and FP4
+ * requantization into the down projection's activation format:
+ *   gate = bf16(alpha_g * A Wg^T), up = bf16(alpha_u * A Wu^T),
+ *   s = bf16( gate * sigmoid(gate) * up ),  S = NVFP4(s) with scale g_inter.
+ * Source: "CUDA: NVFP4 prefill on Blackwell leaves ~1.45x performance on the
+ * table" item 2 (GLU output quantized directly into the next GEMM's
+ * activation format; gate and up share one quantized input).
+ *   A            [T x K] quantized input, shared by both GEMMs.
+ *   W_gate, W_up [I x K] each, same shape.
+ *   inter_mode   NVFP4_INTER_STATIC (g_inter read) or NVFP4_INTER_DYNAMIC
+ *                (g_inter written with the per-call scale).
+ *   s_codes      [T][ld_s_codes] bytes (I/2 per row); s_sf nvfp4_sf_bytes(T, I).
+ *   s_bf16       NULL, or bf16 [T x I] (pitch I): receives s (export).
+ *   workspace    nvfp4_swiglu_workspace_bytes(T, I, inter_mode), 256-B aligned,
+ *                zero-filled once after allocation (calls leave it zeroed).
+ * Requires I % 128 == 0, K % 64 == 0.
+ */
+int nvfp4_gemm_swiglu(const nvfp4_tensor_t* A, const nvfp4_tensor_t* W_gate,
+                      const nvfp4_tensor_t* W_up, int inter_mode, float* g_inter,
+                      uint8_t* s_codes, int64_t ld_s_codes, uint8_t* s_sf, void* s_bf16,
+                      void* workspace, size_t workspace_bytes, nvfp4_stream_t stream);
+
+/*
+ * nvfp4_mlp -- the whole NVFP4 MLP block for a batch of T tokens in one
+ * launch set, activations device-resident, no host synchronisation:
+ *   h   = NVFP4( RMSNorm(x; norm_w, eps) )   (scale g_h computed on device)
+ *   S   = nvfp4_gemm_swiglu(h, W_gate, W_up, inter_mode, g_inter)
+ *   out = bf16( [x +] alpha_d * S W_down^T )
+ * Sources: all three pages (see top of file).
+ *   x        bf16 [T x H], pitch ldx.
+ *   W_gate, W_up [I x H]; W_down [H x I].
+ *   out      bf16 [T x H], pitch ldo; may alias x (in-place residual, ldo == ldx).
+ *   workspace nvfp4_mlp_workspace_bytes(T, H, I, inter_mode), 256-B aligned,
+ *            zero-filled once after allocation (calls leave it zeroed).
+ * Requires H % 64 == 0, I % 128 == 0, T >= 1.
+ */
+int nvfp4_mlp(const void* x, int64_t T, int64_t H, int64_t ldx,
+              const void* norm_w, float eps,
+              const nvfp4_tensor_t* W_gate, const nvfp4_tensor_t* W_up,
+              const nvfp4_tensor_t* W_down, int inter_mode, float* g_inter,
+              void* out, int64_t ldo, int add_residual,
+              void* workspace, size_t workspace_bytes, nvfp4_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NVFP4_H */

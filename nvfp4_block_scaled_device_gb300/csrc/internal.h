@@ -1,0 +1,72 @@
+// Internal (C++) launcher interface between the C-ABI layer and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace nvfp4 {
+
+// Block size of the row kernels (amax / quantize).  Both kernels reduce a
+// row's sum of squares with this many threads in the same order, so the
+// RMSNorm they compute is bit-identical.
+constexpr int kRowThreads = 256;
+
+// Workspace words used by the amax reduction: [0] amax bits, [1] ticket.
+constexpr size_t kAmaxWorkspaceBytes = 8;
+
+cudaError_t launch_amax_scale(const __nv_bfloat16* x, int64_t rows, int64_t cols, int64_t ldx,
+                              const __nv_bfloat16* norm_w, float eps, float* g_out, uint32_t* ws,
+                              int num_sms, cudaStream_t stream);
+
+cudaError_t launch_quantize(const __nv_bfloat16* x, int64_t rows, int64_t cols, int64_t ldx,
+                            const __nv_bfloat16* norm_w, float eps, const float* g, uint8_t* codes,
+                            int64_t ld_codes, uint8_t* sf, __nv_bfloat16* y_out, cudaStream_t stream);
+
+// g_out = max(amax(ws), 1e-8) / 2688, and the amax word is reset to zero.
+cudaError_t launch_finalize_scale(uint32_t* ws, float* g_out, cudaStream_t stream);
+
+enum EpilogueKind : int {
+    kEpiBf16 = 0,        // out = bf16(alpha * acc) [+ residual]
+    kEpiSwigluFp4 = 1,   // s = SwiGLU(gate, up) requantized to FP4 with a given scale
+    kEpiSwigluBf16 = 2,  // s stored as bf16 + its amax accumulated into a workspace word
+};
+
+struct GemmArgs {
+    int epilogue;
+    int64_t M, N, K;  // N: output columns (kEpiBf16) or intermediate columns (SwiGLU)
+    // scale factors (swizzled) and global scales of A and of the B operand(s)
+    const uint8_t* sfa;
+    const uint8_t* sfb0;
+    const uint8_t* sfb1;
+    int64_t sfa_tile_stride;  // bytes between consecutive 128-row scale tiles
+    int64_t sfb_tile_stride;
+    const float* ga;
+    const float* gb0;
+    const float* gb1;
+    // kEpiBf16
+    __nv_bfloat16* out;
+    int64_t ldo;
+    const __nv_bfloat16* residual;
+    int64_t ldr;
+    // SwiGLU epilogues
+    const float* g_inter;
+    uint8_t* s_codes;
+    int64_t ld_s_codes;
+    uint8_t* s_sf;
+    int64_t s_kb_pad;
+    __nv_bfloat16* s_bf16;
+    int64_t ld_s;
+    uint32_t* amax_ws;
+    int* status;
+};
+
+// maps: A [M x K/2 bytes], B0 and B1 (B1 only for SwiGLU) with a 128x128-byte
+// box and 128-byte swizzle.
+cudaError_t launch_gemm(const CUtensorMap& map_a, const CUtensorMap& map_b0, const CUtensorMap& map_b1,
+                        const GemmArgs& args, int num_sms, cudaStream_t stream);
+
+size_t gemm_smem_bytes();
+
+}  // namespace nvfp4

@@ -14,7 +14,9 @@ FP4 codes as packed ``uint8`` [rows, cols/2], scales as LOGICAL ``uint8``
 from __future__ import annotations
 
 import ctypes
+import hashlib
 import os
+import platform
 import subprocess
 import threading
 
@@ -32,12 +34,20 @@ CFLAGS = ["-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fopenmp",
 
 
 def build(force: bool = False) -> str:
-    """Compile the oracle with gcc (seconds).  Returns the library path."""
+    """Compile the oracle with gcc (seconds) unless a library built from the
+    same source on this machine architecture exists.  Returns its path."""
     os.makedirs(_BUILD_DIR, exist_ok=True)
-    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+    h = hashlib.sha256(platform.machine().encode() + " ".join(CFLAGS).encode())
+    with open(_SRC, "rb") as f:
+        h.update(f.read())
+    stamp = _LIB_PATH + ".stamp"
+    fp = h.hexdigest()
+    if force or not os.path.exists(_LIB_PATH) or not os.path.exists(stamp) or open(stamp).read() != fp:
         tmp = _LIB_PATH + f".tmp{os.getpid()}"
         subprocess.check_call(["gcc", *CFLAGS, _SRC, "-o", tmp, "-lm"])
         os.replace(tmp, _LIB_PATH)
+        with open(stamp, "w") as f:
+            f.write(fp)
     return _LIB_PATH
 
 

@@ -1,0 +1,102 @@
+"""Host-side tests of the C ABI (no GPU needed): the library builds and loads,
+exports every function include/nvfp4.h declares, its size helpers agree with
+the documented layout, and invalid arguments are rejected before any CUDA
+call is made."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from nvfp4_block_scaled_device_gb300 import build
+    build.build()
+    import nvfp4_block_scaled_device_gb300 as nv
+    return nv.lib()
+
+
+def header_functions():
+    src = open(os.path.join(ROOT, "include", "nvfp4.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(nvfp4_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_header_declares_the_four_path_entry_points():
+    names = header_functions()
+    for n in ("nvfp4_amax_scale", "nvfp4_quantize", "nvfp4_gemm", "nvfp4_mlp"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    names = header_functions()
+    assert names
+    for n in names:
+        assert hasattr(L, n), n
+    import nvfp4_block_scaled_device_gb300 as nv
+    assert set(names) == set(nv.EXPORTED_FUNCTIONS)
+
+
+def test_size_helpers(L):
+    import nvfp4_block_scaled_device_gb300 as nv
+    assert nv.codes_bytes(16, 256) == 16 * 128
+    assert nv.sf_bytes(16, 256) == 128 * 16
+    assert nv.sf_bytes(128, 64) == 128 * 4
+    assert nv.sf_bytes(129, 5120) == 256 * 320
+    assert nv.sf_bytes(1, 17408) == 128 * 1088
+    assert nv.amax_workspace_bytes() >= 8
+    assert nv.swiglu_workspace_bytes(1024, 17408, nv.NVFP4_INTER_DYNAMIC) >= 1024 * 17408 * 2
+    assert nv.mlp_workspace_bytes(1024, 5120, 17408, nv.NVFP4_INTER_STATIC) >= (
+        1024 * 2560 + 1024 * 320 + 1024 * 8704 + 1024 * 1088)
+
+
+def test_status_strings(L):
+    for s in range(7):
+        assert L.nvfp4_status_string(s)
+    assert L.nvfp4_status_string(0) == b"ok"
+
+
+def test_invalid_arguments_rejected_on_host(L):
+    import nvfp4_block_scaled_device_gb300 as nv
+    NULL = None
+    # NULL tensors
+    assert L.nvfp4_gemm(NULL, NULL, NULL, 0, NULL, 0, NULL) == 1
+    # bad shapes: cols not a multiple of 64
+    a = nv._TensorC(16, 128 * 16, 4, 16, 100, 64)
+    w = nv._TensorC(16, 128 * 16, 4, 512, 100, 64)
+    assert L.nvfp4_gemm(ctypes.byref(a), ctypes.byref(w), 16, 512, NULL, 0, NULL) == 1
+    # misaligned codes pointer
+    a = nv._TensorC(17, 128 * 16, 4, 16, 256, 128)
+    w = nv._TensorC(16, 128 * 16, 4, 512, 256, 128)
+    assert L.nvfp4_gemm(ctypes.byref(a), ctypes.byref(w), 16, 512, NULL, 0, NULL) == 2
+    # K mismatch
+    a = nv._TensorC(16, 128 * 16, 4, 16, 256, 128)
+    w = nv._TensorC(16, 128 * 16, 4, 512, 512, 256)
+    assert L.nvfp4_gemm(ctypes.byref(a), ctypes.byref(w), 16, 512, NULL, 0, NULL) == 1
+    # quantize: cols % 64
+    assert L.nvfp4_quantize(16, 4, 32, 32, NULL, 1e-6, 16, 16, 16, 128, NULL, NULL) == 1
+    # amax: missing workspace
+    assert L.nvfp4_amax_scale(16, 4, 64, 64, NULL, 1e-6, 16, NULL, 0, NULL) == 5
+    # mlp: bad inter mode
+    t = nv._TensorC(16, 128, 4, 256, 256, 128)
+    assert L.nvfp4_mlp(16, 4, 256, 256, 16, 1e-6, ctypes.byref(t), ctypes.byref(t), ctypes.byref(t), 7, 16,
+                       16, 256, 1, 256, 1 << 30, NULL) == 1
+
+
+def test_python_binding_fails_loudly_without_library(tmp_path):
+    import nvfp4_block_scaled_device_gb300 as nv
+    with pytest.raises(RuntimeError):
+        nv.lib(str(tmp_path / "missing.so"))
+
+
+def test_product_path_does_not_import_oracle():
+    pkg = os.path.join(ROOT, "nvfp4_block_scaled_device_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".c")):
+                src = open(os.path.join(dirpath, f)).read()
+                assert not re.search(r"^\s*(import|from)\s+oracle", src, flags=re.M), f
+                assert "liboracle" not in src and "nvfp4_oracle" not in src, f

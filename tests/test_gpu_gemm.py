@@ -1,0 +1,135 @@
+"""GPU parity of the tcgen05 block-scaled GEMM against the oracle's exact
+(int64) dot products.  The GPU quantizes the operands itself; each test first
+asserts those operands are bit-identical to the oracle's own quantization of
+the same bf16 inputs, then compares the GEMM output within the tolerance
+(rel. Frobenius <= 5e-3; |err| <= 2^-7 |ref| + 1e-3 sum|a w|)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synthetic
+from _gpu import assert_same_quant, check_close, dev, f64, host, oracle_quant, quantize_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def nv():
+    import __graft_entry__
+    __graft_entry__.build()
+    import nvfp4_block_scaled_device_gb300 as m
+    return m
+
+
+@pytest.fixture()
+def ws(nv):
+    return nv.workspace(256)
+
+
+def run_case(nv, ws, M, N, K, seed, residual=False, a_outliers=False):
+    rng = np.random.default_rng(seed)
+    if a_outliers:
+        a = synthetic.student_t_outliers(rng, (M, K))
+    else:
+        a = synthetic.normal(rng, (M, K))
+    w = synthetic.normal(rng, (N, K), std=0.02)
+    A, W = quantize_gpu(a, ws), quantize_gpu(w, ws)
+    ac, asf, ga = oracle_quant(a)
+    wc, wsf, gw = oracle_quant(w)
+    assert_same_quant(A, ac, asf, ga, "A")
+    assert_same_quant(W, wc, wsf, gw, "W")
+    res_bits = synthetic.normal(rng, (M, N)) if residual else None
+    out = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    nv.nvfp4_gemm(A, W, out, residual=None if res_bits is None else dev(res_bits))
+    torch.cuda.synchronize()
+    assert nv.device_status() == 0
+    ref, absref, out_bits = oracle.gemm(ac, asf, ga, wc, wsf, gw, residual=res_bits)
+    got = f64(host(out))
+    if residual:
+        ref = ref + f64(res_bits)
+    return got, ref, absref
+
+
+def test_single_linear_16x512x256(nv, ws):
+    """A 16x256 ~N(0,1), W 512x256 ~N(0,0.02), seed 0 (one stream)."""
+    a, w = synthetic.single_linear(16, 512, 256, seed=0)
+    A, W = quantize_gpu(a, ws), quantize_gpu(w, ws)
+    ac, asf, ga = oracle_quant(a)
+    wc, wsf, gw = oracle_quant(w)
+    assert_same_quant(A, ac, asf, ga, "A")
+    assert_same_quant(W, wc, wsf, gw, "W")
+    out = torch.empty((16, 512), dtype=torch.bfloat16, device="cuda")
+    nv.nvfp4_gemm(A, W, out)
+    ref, absref, _ = oracle.gemm(ac, asf, ga, wc, wsf, gw)
+    check_close(f64(host(out)), ref, absref, "16x512x256")
+
+
+@pytest.mark.parametrize("M,N,K", [
+    (1, 256, 64), (3, 512, 192), (17, 384, 320), (128, 256, 256), (130, 512, 512),
+    (16, 16, 256), (200, 1024, 1024), (777, 512, 5120), (64, 768, 17408 // 4),
+])
+def test_ragged_shapes(nv, ws, M, N, K):
+    got, ref, absref = run_case(nv, ws, M, N, K, seed=M + N + K)
+    check_close(got, ref, absref, f"{M}x{N}x{K}")
+
+
+def test_residual_add(nv, ws):
+    got, ref, absref = run_case(nv, ws, 33, 512, 256, seed=5, residual=True)
+    check_close(got, ref, absref + np.abs(ref) * 0, "residual")
+
+
+def test_residual_in_place(nv, ws):
+    rng = np.random.default_rng(6)
+    a = synthetic.normal(rng, (40, 256))
+    w = synthetic.normal(rng, (256, 256), std=0.02)
+    r = synthetic.normal(rng, (40, 256))
+    A, W = quantize_gpu(a, ws), quantize_gpu(w, ws)
+    buf = dev(r)
+    nv.nvfp4_gemm(A, W, buf, residual=buf)
+    ac, asf, ga = oracle_quant(a)
+    wc, wsf, gw = oracle_quant(w)
+    ref, absref, _ = oracle.gemm(ac, asf, ga, wc, wsf, gw)
+    check_close(f64(host(buf)), ref + f64(r), absref, "in-place residual")
+
+
+def test_outlier_activations(nv, ws):
+    got, ref, absref = run_case(nv, ws, 64, 512, 5120, seed=11, a_outliers=True)
+    check_close(got, ref, absref, "outliers")
+
+
+def test_deterministic(nv, ws):
+    rng = np.random.default_rng(12)
+    A = quantize_gpu(synthetic.normal(rng, (300, 1024)), ws)
+    W = quantize_gpu(synthetic.normal(rng, (768, 1024), std=0.02), ws)
+    o1 = torch.empty((300, 768), dtype=torch.bfloat16, device="cuda")
+    o2 = torch.empty_like(o1)
+    nv.nvfp4_gemm(A, W, o1)
+    nv.nvfp4_gemm(A, W, o2)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2)
+
+
+@pytest.mark.parametrize("M,N,K", [(1024, 7168, 5120), (1024, 5120, 17408), (1, 5120, 17408)])
+def test_full_size_sampled(nv, ws, M, N, K):
+    """Full projection sizes of the 27B-class model (QKV, down): quantized
+    operands compared in full, GEMM outputs on 2048 sampled elements."""
+    rng = np.random.default_rng(M + N)
+    a = synthetic.normal(rng, (M, K))
+    w = synthetic.normal(rng, (N, K), std=0.02)
+    A, W = quantize_gpu(a, ws), quantize_gpu(w, ws)
+    out = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    nv.nvfp4_gemm(A, W, out)
+    ac, asf, ga = oracle_quant(a)
+    wc, wsf, gw = oracle_quant(w)
+    assert_same_quant(A, ac, asf, ga, "A")
+    assert_same_quant(W, wc, wsf, gw, "W")
+    m = rng.integers(0, M, 2048)
+    n = rng.integers(0, N, 2048)
+    # always include the last row / column tiles
+    m[:8] = M - 1
+    n[8:16] = N - 1
+    dot, adot = oracle.dot_sampled(ac, asf, wc, wsf, m, n)
+    alpha = float(np.float32(np.float32(ga) * np.float32(gw)))
+    got = f64(host(out))[m, n]
+    check_close(got, alpha * dot, alpha * adot, f"{M}x{N}x{K} sampled")

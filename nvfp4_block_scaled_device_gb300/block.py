@@ -1,0 +1,104 @@
+"""One prefill layer block of NVFP4 linears as a single launch set.
+
+For a ubatch of T tokens (hidden H, intermediate I, QKV width N_qkv):
+
+    h   = NVFP4(RMSNorm(x; attn_norm))            device scale, no host sync
+    qkv = h @ Wqkv^T                              bf16 [T x N_qkv]
+    a   = NVFP4(qkv[:, :H])                       attention-core stand-in: the
+                                                  Q slice passes through unchanged
+    x1  = x + a @ Wo^T                            residual fused in the epilogue
+    out = x1 + MLP(x1)                            nvfp4_mlp (RMSNorm prologue,
+                                                  fused gate/up SwiGLU + FP4
+                                                  requant, down + residual)
+
+Sources: "tp>1 prefill is host-bound" (vllm.cpp issue 2144) fix directions
+1-3 -- one launch set per T-token batch, activations resident on the device,
+quantization on the device; "PERFORMANCE -- verified hot-path audit and
+prioritized fixes" P0 fix 1 -- the intermediate scale is fixed once by a
+warm-up ubatch and kept on the device (``calibrate``), P8 item 5 -- with no
+host synchronisation the launch set can be captured in a CUDA graph.
+The attention core itself is outside this path; the identity stand-in keeps
+the O projection's input shape and statistics of a real attention output.
+
+Every launch is a libnvfp4 call; this module only holds buffers and
+sequences calls.  All buffers are allocated at construction.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import (NVFP4_INTER_DYNAMIC, NVFP4_INTER_STATIC, NVFP4Tensor, mlp_workspace_bytes, nvfp4_amax_scale,
+               nvfp4_gemm, nvfp4_gemm_swiglu, nvfp4_mlp, nvfp4_quantize, swiglu_workspace_bytes, workspace)
+
+
+class PrefillBlock:
+    LAUNCHES_PER_FORWARD = 10  # 2 norm+quant, 1 QKV, 2 stand-in quant, 1 O, 4 MLP (static scale)
+
+    def __init__(self, T: int, weights: dict, attn_norm: torch.Tensor, mlp_norm: torch.Tensor, eps=1e-6):
+        """weights: NVFP4Tensor values under 'qkv' [Nqkv x H], 'o' [H x H],
+        'gate', 'up' [I x H], 'down' [H x I]."""
+        self.T = T
+        self.w = weights
+        self.H = weights["o"].rows
+        self.I = weights["gate"].rows
+        self.Nqkv = weights["qkv"].rows
+        self.attn_norm, self.mlp_norm, self.eps = attn_norm, mlp_norm, eps
+        dev = attn_norm.device
+        H, I = self.H, self.I
+        self.h = NVFP4Tensor.empty(T, H, dev)
+        self.a = NVFP4Tensor.empty(T, H, dev)
+        self.qkv = torch.empty((T, self.Nqkv), dtype=torch.bfloat16, device=dev)
+        self.x1 = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+        self.g_inter = torch.ones((1,), dtype=torch.float32, device=dev)
+        self.ws_amax = workspace(256, dev)
+        self.ws_mlp = workspace(mlp_workspace_bytes(T, H, I, NVFP4_INTER_DYNAMIC), dev)
+        # buffers of the decomposed MLP (same kernels as nvfp4_mlp, with a
+        # launch boundary exposed between them for per-kernel timing)
+        self.hm = NVFP4Tensor.empty(T, H, dev)
+        self.s = NVFP4Tensor.empty(T, I, dev)
+        self.s.g = self.g_inter          # the intermediate carries the intermediate scale
+        self.ws_swiglu = workspace(swiglu_workspace_bytes(T, I, NVFP4_INTER_STATIC), dev)
+
+    def attention_part(self, x: torch.Tensor, stream=None, ev=None):
+        rec = (lambda k: ev[k].record(stream)) if ev is not None else (lambda k: None)
+        nvfp4_amax_scale(x, self.h.g, self.ws_amax, self.attn_norm, self.eps, stream)
+        nvfp4_quantize(x, self.h.g, self.h, self.attn_norm, self.eps, None, stream)
+        rec("qkv0")
+        nvfp4_gemm(self.h, self.w["qkv"], self.qkv, None, stream)
+        rec("qkv1")
+        q = self.qkv[:, :self.H]
+        nvfp4_amax_scale(q, self.a.g, self.ws_amax, None, self.eps, stream)
+        nvfp4_quantize(q, self.a.g, self.a, None, self.eps, None, stream)
+        rec("o0")
+        nvfp4_gemm(self.a, self.w["o"], self.x1, x, stream)
+        rec("o1")
+
+    def calibrate(self, x: torch.Tensor, out: torch.Tensor, stream=None):
+        """One ubatch with the per-call intermediate scale; leaves that scale
+        in self.g_inter (on the device) for the STATIC launches that follow."""
+        self.attention_part(x, stream)
+        nvfp4_mlp(self.x1, self.mlp_norm, self.w["gate"], self.w["up"], self.w["down"], NVFP4_INTER_DYNAMIC,
+                  self.g_inter, out, self.ws_mlp, True, self.eps, stream)
+
+    def forward(self, x: torch.Tensor, out: torch.Tensor, stream=None):
+        """x, out: bf16 [T x H] (may alias)."""
+        self.attention_part(x, stream)
+        nvfp4_mlp(self.x1, self.mlp_norm, self.w["gate"], self.w["up"], self.w["down"], NVFP4_INTER_STATIC,
+                  self.g_inter, out, self.ws_mlp, True, self.eps, stream)
+
+    def forward_timed(self, x: torch.Tensor, out: torch.Tensor, ev: dict, stream=None):
+        """forward() with the MLP launched through its parts (the same four
+        kernels nvfp4_mlp launches) and CUDA events around each GEMM."""
+        rec = lambda k: ev[k].record(stream)
+        self.attention_part(x, stream, ev)
+        rec("mlp0")
+        nvfp4_amax_scale(self.x1, self.hm.g, self.ws_amax, self.mlp_norm, self.eps, stream)
+        nvfp4_quantize(self.x1, self.hm.g, self.hm, self.mlp_norm, self.eps, None, stream)
+        rec("gu0")
+        nvfp4_gemm_swiglu(self.hm, self.w["gate"], self.w["up"], NVFP4_INTER_STATIC, self.g_inter, self.s,
+                          self.ws_swiglu, None, stream)
+        rec("gu1")
+        nvfp4_gemm(self.s, self.w["down"], out, self.x1, stream)
+        rec("dn1")
+
+    EVENT_NAMES = ("qkv0", "qkv1", "o0", "o1", "mlp0", "gu0", "gu1", "dn1")

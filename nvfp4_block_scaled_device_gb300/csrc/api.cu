@@ -396,4 +396,9 @@ int nvfp4_mlp(const void* x, int64_t T, int64_t H, int64_t ldx, const void* norm
     return NVFP4_OK;
 }
 
+#ifdef NVFP4_TRACE
+// Debug builds only: copy the GEMM timeline of CTA 0 to the host.
+int nvfp4_debug_trace(unsigned long long* out, int n);
+#endif
+
 }  // extern "C"

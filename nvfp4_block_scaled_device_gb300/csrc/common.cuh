@@ -13,9 +13,6 @@ namespace nvfp4 {
 // Error code written to the device status word when a wait gives up; the
 // value is kErrTimeout * 100 + a site number.
 constexpr int kErrTimeout = 6;
-// Upper bound on any single pipeline wait (ns of %globaltimer).  Legitimate
-// waits are microseconds; this only turns a would-be hang into an error.
-constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p)
 {
@@ -74,23 +71,54 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
     return ok != 0;
 }
 
-// Wait for phase `parity` of an mbarrier, giving up after kWaitLimitNs or
-// as soon as another warp of the CTA has given up (`abort_flag` != 0).
-// On giving up it raises the CTA's abort flag and records
-// kErrTimeout*100 + site in the device status word; returns false.
+// try_wait that may suspend the thread (no issue slots used) for up to
+// `hint_ns` while the phase is incomplete; it returns as soon as the phase
+// completes.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n"
+        " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+        " selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait for phase `parity` of an mbarrier, giving up after about
+// kWaitLimitCycles SM clock cycles (~2 s) or as soon as another warp of the
+// CTA has given up (`abort_flag` != 0).  On giving up it raises the CTA's
+// abort flag and records kErrTimeout*100 + site in the device status word;
+// returns false.  The limit uses the SM cycle counter (cheap to read) and is
+// checked only every 64 polls, so a healthy wait costs only try_wait polls.
+constexpr uint64_t kWaitLimitCycles = 4000000000ull;
+
+template <bool kSleep = false>
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                           int* status, int site)
 {
     if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer();
-    while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if (*abort_flag) return false;
-        if (globaltimer() - t0 > kWaitLimitNs) {
-            *abort_flag = 1;
-            if (status) atomicCAS(status, 0, kErrTimeout * 100 + site);
-            return false;
+    const uint64_t t0 = clock64();
+    for (uint32_t i = 1;; i++) {
+        if (kSleep ? mbar_try_wait_sleep(bar, parity, 20000u) : mbar_try_wait(bar, parity)) return true;
+        if ((i & 63u) == 0) {
+            if (*abort_flag) return false;
+            if ((uint64_t)(clock64() - t0) > kWaitLimitCycles) {
+                *abort_flag = 1;
+                if (status) atomicCAS(status, 0, kErrTimeout * 100 + site);
+                return false;
+            }
         }
+    }
+}
+
+// Bounded wait that ignores the abort flag (used while tearing down).
+__device__ __forceinline__ void mbar_wait_teardown(uint32_t bar, uint32_t parity)
+{
+    const uint64_t t0 = clock64();
+    while (!mbar_try_wait(bar, parity) && (uint64_t)(clock64() - t0) < kWaitLimitCycles / 8) {
     }
 }
 
@@ -103,6 +131,21 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
         " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "l"(cache_hint)
         : "memory");
+}
+
+// Warm L2 with a tensor tile (no shared-memory destination, no completion).
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int32_t x, int32_t y)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y)
+                 : "memory");
+}
+
+// Warm L2 with a contiguous range (16-B aligned, size % 16 == 0).
+__device__ __forceinline__ void bulk_prefetch(const void* src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
 // 1-D bulk copy global -> shared (16-B aligned addresses, size % 16 == 0).
@@ -173,6 +216,11 @@ __device__ __forceinline__ uint64_t make_smem_desc(uint32_t start, uint32_t lbo,
     return d;
 }
 
+__device__ __forceinline__ uint64_t desc_from(uint32_t lo, uint32_t hi)
+{
+    return ((uint64_t)hi << 32) | lo;
+}
+
 // Block-scaled MMA: D[tmem] (+)= A[smem] * B[smem]^T with per-16 UE4M3
 // scales of A and B read from tensor memory; E2M1 operands, fp32 accumulate.
 __device__ __forceinline__ void mma_mxf4nvf4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
@@ -192,6 +240,83 @@ __device__ __forceinline__ void mma_mxf4nvf4(uint32_t d_tmem, uint64_t a_desc, u
 __device__ __forceinline__ void tmem_copy_sf(uint32_t taddr, uint64_t src_desc)
 {
     asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(src_desc) : "memory");
+}
+
+// ---- warp-wide issue: the whole (converged) warp executes these; one
+// elected lane (the lowest active lane, the same in every call) issues.
+// Issuing tcgen05 and TMA instructions from a converged warp lets them
+// pipeline; from a lone lane of a diverged warp each one stalls the issuer
+// for roughly the instruction's execution time.
+__device__ __forceinline__ void mma_mxf4nvf4_warp(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                                  uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n .reg .pred p, e;\n .reg .b32 r;\n"
+        " setp.ne.b32 p, %6, 0;\n"
+        " elect.sync r|e, 0xffffffff;\n"
+        " @e tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n"
+        "}\n" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_copy_sf_warp(uint32_t taddr, uint64_t src_desc)
+{
+    asm volatile(
+        "{\n .reg .pred e;\n .reg .b32 r;\n elect.sync r|e, 0xffffffff;\n"
+        " @e tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;\n}" ::"r"(taddr),
+        "l"(src_desc)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_commit_warp(uint32_t bar)
+{
+    asm volatile(
+        "{\n .reg .pred e;\n .reg .b32 r;\n elect.sync r|e, 0xffffffff;\n"
+        " @e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}" ::"r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx_warp(uint32_t bar, uint32_t bytes)
+{
+    asm volatile(
+        "{\n .reg .pred e;\n .reg .b32 r;\n elect.sync r|e, 0xffffffff;\n"
+        " @e mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n}" ::"r"(bar),
+        "r"(bytes)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d_warp(uint32_t dst, const CUtensorMap* map, uint32_t bar, int32_t x,
+                                                 int32_t y, uint64_t cache_hint)
+{
+    asm volatile(
+        "{\n .reg .pred e;\n .reg .b32 r;\n elect.sync r|e, 0xffffffff;\n"
+        " @e cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%3, %4}], [%2], %5;\n}" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "l"(cache_hint)
+        : "memory");
+}
+
+__device__ __forceinline__ void bulk_load_warp(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar)
+{
+    asm volatile(
+        "{\n .reg .pred e;\n .reg .b32 r;\n elect.sync r|e, 0xffffffff;\n"
+        " @e cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n}" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+// Warp-wide bounded wait: lane 0 polls, the result is broadcast and the
+// warp leaves converged.
+template <bool kSleep = false>
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* status,
+                                               int site)
+{
+    int ok = 1;
+    if ((threadIdx.x & 31) == 0) ok = mbar_wait<kSleep>(bar, parity, abort_flag, status, site) ? 1 : 0;
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    __syncwarp();
+    return ok != 0;
 }
 
 // Arrive on an mbarrier once all tcgen05 operations issued so far by this

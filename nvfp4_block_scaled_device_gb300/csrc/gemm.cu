@@ -51,18 +51,22 @@ static_assert(kAccCols + kStages * kSfColsPerStage <= kTmemCols, "tensor memory 
 constexpr int kNumThreads = 320;
 constexpr int kEpiWarps = 8;
 
-// Width of one MMA instruction: 256 (the 256 B rows in one instruction) or
-// 128 (two instructions, one per 128-row half of B).
-#ifndef NVFP4_MMA_N
-#define NVFP4_MMA_N 256
-#endif
-constexpr uint32_t kMmaN = NVFP4_MMA_N;
-static_assert(kMmaN == 256 || kMmaN == 128, "MMA width");
-
 // Instruction descriptor, kind::mxf4nvf4: A and B E2M1 (format 1), UE4M3
-// scales (bit 23 = 0), K-major A and B, N (bits 17-22 = N/8),
+// scales (bit 23 = 0), K-major A and B, N = 256 (bits 17-22 = N/8),
 // M = 128 (bits 24-28 = M/16), dense, scale-factor ids 0.
-constexpr uint32_t kIdesc = (1u << 7) | (1u << 10) | ((kMmaN >> 3) << 17) | ((128u >> 4) << 24);
+constexpr uint32_t kIdesc = (1u << 7) | (1u << 10) | ((256u >> 3) << 17) | ((128u >> 4) << 24);
+
+#ifdef NVFP4_TRACE
+// Debug timeline of CTA 0 (built only with -DNVFP4_TRACE): SM clock at each
+// pipeline handoff.  [0,256) producer empty-wait done, [256,512) producer
+// issued, [512,768) MMA full-wait done, [768,1024) MMA issued, [1024,1088)
+// MMA acc-empty done, [1088,1152) epilogue acc-full done, [1152,1216) drained.
+__device__ unsigned long long g_trace[1216];
+#define TRACE(slot, i) \
+    do { if (blockIdx.x == 0 && (i) < 64 * ((slot) < 1024 ? 4 : 1)) g_trace[(slot) + (i)] = clock64(); } while (0)
+#else
+#define TRACE(slot, i) do { } while (0)
+#endif
 
 struct Ctrl {
     uint64_t full[kStages];
@@ -74,6 +78,25 @@ struct Ctrl {
     int abort_flag;
 };
 static_assert(sizeof(Ctrl) <= kCtrlBytes, "control block");
+
+// The 12 scale-tile copies of a full stage (A, B rows 0-127, B rows
+// 128-255, for each of 4 K-steps), straight-line.
+__device__ __forceinline__ void issue_sf4(uint32_t c, uint32_t f, uint32_t hi)
+{
+    constexpr uint32_t kB0 = kSfaBytes >> 4, kB1 = (kSfaBytes + 4 * kSfTile) >> 4, kT = kSfTile >> 4;
+    tmem_copy_sf_warp(c, desc_from(f, hi));
+    tmem_copy_sf_warp(c + 4, desc_from(f + kB0, hi));
+    tmem_copy_sf_warp(c + 8, desc_from(f + kB1, hi));
+    tmem_copy_sf_warp(c + kSfColsPerKK, desc_from(f + kT, hi));
+    tmem_copy_sf_warp(c + kSfColsPerKK + 4, desc_from(f + kT + kB0, hi));
+    tmem_copy_sf_warp(c + kSfColsPerKK + 8, desc_from(f + kT + kB1, hi));
+    tmem_copy_sf_warp(c + 2 * kSfColsPerKK, desc_from(f + 2 * kT, hi));
+    tmem_copy_sf_warp(c + 2 * kSfColsPerKK + 4, desc_from(f + 2 * kT + kB0, hi));
+    tmem_copy_sf_warp(c + 2 * kSfColsPerKK + 8, desc_from(f + 2 * kT + kB1, hi));
+    tmem_copy_sf_warp(c + 3 * kSfColsPerKK, desc_from(f + 3 * kT, hi));
+    tmem_copy_sf_warp(c + 3 * kSfColsPerKK + 4, desc_from(f + 3 * kT + kB0, hi));
+    tmem_copy_sf_warp(c + 3 * kSfColsPerKK + 8, desc_from(f + 3 * kT + kB1, hi));
+}
 
 __device__ __forceinline__ float silu_mul(float gate, float up)
 {
@@ -128,125 +151,167 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 
     if (warp == 0) {
         // ------------------------------------------------------ producer
-        if (lane == 0) {
-            const uint64_t pol_a = l2_policy_evict_last();
-            const uint64_t pol_b = l2_policy_evict_first();
-            int s = 0;
-            uint32_t ph = 0, issued = 0, issued_ph = 0;
-            bool ok = true;
-            for (int64_t tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-                const int64_t mt = tile % num_m, nt = tile / num_m;
-                const int32_t ya = (int32_t)(mt * 128);
-                int32_t yb0, yb1;
-                const uint8_t *sfb0_src, *sfb1_src;
-                bool has_b1;
-                if (swiglu) {
-                    yb0 = yb1 = (int32_t)(nt * 128);
-                    sfb0_src = args.sfb0 + nt * args.sfb_tile_stride;
-                    sfb1_src = args.sfb1 + nt * args.sfb_tile_stride;
-                    has_b1 = true;
-                } else {
-                    yb0 = (int32_t)(nt * 256);
-                    yb1 = yb0 + 128;
-                    sfb0_src = args.sfb0 + (2 * nt) * args.sfb_tile_stride;
-                    sfb1_src = args.sfb0 + (2 * nt + 1) * args.sfb_tile_stride;
-                    has_b1 = yb1 < args.N;   // else the scale tile does not exist
-                }
-                const uint8_t* sfa_src = args.sfa + mt * args.sfa_tile_stride;
-                const CUtensorMap* mb1 = swiglu ? &map_b1 : &map_b0;
-                for (int kb = 0; kb < num_kstages; kb++) {
-                    if (!mbar_wait(smem_u32(&ctrl->empty[s]), ph ^ 1u, abort_flag, args.status, 1)) {
-                        ok = false;
-                        break;
-                    }
-                    const int nkk = min(4, num_kk - kb * 4);
-                    const uint32_t sf_bytes = (uint32_t)nkk * kSfTile;
-                    // a B half entirely past N is not loaded: its stale shared
-                    // memory only feeds accumulator columns >= N, never stored
-                    const uint32_t tx = kABytes + kBHalfBytes * (has_b1 ? 2u : 1u) + sf_bytes * (has_b1 ? 3u : 2u);
-                    const uint32_t full = smem_u32(&ctrl->full[s]);
-                    mbar_arrive_expect_tx(full, tx);
-                    const uint32_t st = base + (uint32_t)(s * kStageBytes);
-                    const int32_t xk = kb * 128;
-                    tma_load_2d(st, &map_a, full, xk, ya, pol_a);
-                    tma_load_2d(st + kABytes, &map_b0, full, xk, yb0, pol_b);
-                    if (has_b1) tma_load_2d(st + kABytes + kBHalfBytes, mb1, full, xk, yb1, pol_b);
-                    const uint32_t sf_st = st + kABytes + kBBytes;
-                    bulk_load(sf_st, sfa_src + (int64_t)kb * 4 * kSfTile, sf_bytes, full);
-                    bulk_load(sf_st + kSfaBytes, sfb0_src + (int64_t)kb * 4 * kSfTile, sf_bytes, full);
-                    if (has_b1)
-                        bulk_load(sf_st + kSfaBytes + 4 * kSfTile, sfb1_src + (int64_t)kb * 4 * kSfTile, sf_bytes,
-                                  full);
-                    issued |= 1u << s;
-                    issued_ph = (issued_ph & ~(1u << s)) | (ph << s);
-                    if (++s == kStages) {
-                        s = 0;
-                        ph ^= 1u;
-                    }
-                }
+        // The whole warp runs the loop; one elected lane issues each copy.
+        const uint64_t pol_a = l2_policy_evict_last();
+        const uint64_t pol_b = l2_policy_evict_first();
+        const uint32_t full0 = smem_u32(&ctrl->full[0]);
+        const uint32_t empty0 = smem_u32(&ctrl->empty[0]);
+        int s = 0;
+        uint32_t ph = 0, issued = 0, issued_ph = 0;
+        int kcount = 0;
+        bool ok = true;
+        for (int64_t tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+            const int64_t mt = tile % num_m, nt = tile / num_m;
+            const int32_t ya = (int32_t)(mt * 128);
+            int32_t yb0, yb1;
+            const uint8_t *pb0, *pb1;
+            bool has_b1;
+            if (swiglu) {
+                yb0 = yb1 = (int32_t)(nt * 128);
+                pb0 = args.sfb0 + nt * args.sfb_tile_stride;
+                pb1 = args.sfb1 + nt * args.sfb_tile_stride;
+                has_b1 = true;
+            } else {
+                yb0 = (int32_t)(nt * 256);
+                yb1 = yb0 + 128;
+                pb0 = args.sfb0 + (2 * nt) * args.sfb_tile_stride;
+                pb1 = args.sfb0 + (2 * nt + 1) * args.sfb_tile_stride;
+                has_b1 = yb1 < args.N;   // else the scale tile does not exist
             }
-            if (!ok) {
-                // stopped early: let the copies already issued land before the
-                // CTA's shared memory goes away (bounded)
-                for (int i = 0; i < kStages; i++) {
-                    if (!(issued & (1u << i))) continue;
-                    const uint64_t t0 = globaltimer();
-                    while (!mbar_try_wait(smem_u32(&ctrl->full[i]), (issued_ph >> i) & 1u) &&
-                           globaltimer() - t0 < kWaitLimitNs / 8) {
-                    }
+            const uint8_t* pa = args.sfa + mt * args.sfa_tile_stride;
+            const CUtensorMap* mb1 = swiglu ? &map_b1 : &map_b0;
+            const uint32_t tx_full = kABytes + kBHalfBytes * (has_b1 ? 2u : 1u) + 4u * kSfTile * (has_b1 ? 3u : 2u);
+            for (int kb = 0; kb < num_kstages; kb++) {
+                if (!mbar_wait_warp(empty0 + 8u * (uint32_t)s, ph ^ 1u, abort_flag, args.status, 1)) {
+                    ok = false;
+                    break;
+                }
+                if (lane == 0) TRACE(0, kcount);
+                // a B half entirely past N is not loaded: its stale shared
+                // memory only feeds accumulator columns >= N, never stored
+                const bool tail = kb == num_kstages - 1;
+                const uint32_t sf_bytes = tail ? (uint32_t)(num_kk - kb * 4) * kSfTile : 4u * kSfTile;
+                const uint32_t tx =
+                    tail ? kABytes + kBHalfBytes * (has_b1 ? 2u : 1u) + sf_bytes * (has_b1 ? 3u : 2u) : tx_full;
+                const uint32_t full = full0 + 8u * (uint32_t)s;
+                const uint32_t st = base + (uint32_t)s * kStageBytes;
+                const uint32_t sf_st = st + kABytes + kBBytes;
+                const int32_t xk = kb * 128;
+                mbar_arrive_expect_tx_warp(full, tx);
+                if (has_b1) {   // straight-line common case
+                    tma_load_2d_warp(st, &map_a, full, xk, ya, pol_a);
+                    tma_load_2d_warp(st + kABytes, &map_b0, full, xk, yb0, pol_b);
+                    tma_load_2d_warp(st + kABytes + kBHalfBytes, mb1, full, xk, yb1, pol_b);
+                    bulk_load_warp(sf_st, pa, sf_bytes, full);
+                    bulk_load_warp(sf_st + kSfaBytes, pb0, sf_bytes, full);
+                    bulk_load_warp(sf_st + kSfaBytes + 4 * kSfTile, pb1, sf_bytes, full);
+                } else {
+                    tma_load_2d_warp(st, &map_a, full, xk, ya, pol_a);
+                    tma_load_2d_warp(st + kABytes, &map_b0, full, xk, yb0, pol_b);
+                    bulk_load_warp(sf_st, pa, sf_bytes, full);
+                    bulk_load_warp(sf_st + kSfaBytes, pb0, sf_bytes, full);
+                }
+                pa += 4 * kSfTile;
+                pb0 += 4 * kSfTile;
+                pb1 += 4 * kSfTile;
+                if (lane == 0) TRACE(256, kcount);
+                kcount++;
+                issued |= 1u << s;
+                issued_ph = (issued_ph & ~(1u << s)) | (ph << s);
+                if (++s == kStages) {
+                    s = 0;
+                    ph ^= 1u;
                 }
             }
         }
+        if (!ok && lane == 0) {
+            // stopped early: let the copies already issued land before the
+            // CTA's shared memory goes away (bounded)
+            for (int i = 0; i < kStages; i++)
+                if (issued & (1u << i)) mbar_wait_teardown(full0 + 8u * (uint32_t)i, (issued_ph >> i) & 1u);
+        }
+        __syncwarp();
     } else if (warp == 1) {
         // ----------------------------------------------------------- MMA
-        if (lane == 0) {
-            int s = 0;
-            uint32_t ph = 0, acc_ph = 0;
-            bool ok = true;
-            for (int64_t tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-                if (!mbar_wait(smem_u32(&ctrl->acc_empty), acc_ph ^ 1u, abort_flag, args.status, 2)) break;
+        // The whole warp runs the loop; one elected lane issues the scale
+        // copies, the MMAs and the commits (always the same lane, so each
+        // commit tracks all MMAs before it).
+        // K-major, 128-byte swizzle, 8-row groups 1024 B apart (codes);
+        // no swizzle, 16-byte rows, 8-row groups 128 B apart (scales)
+        const uint64_t dsw = make_smem_desc(base, 16, 1024, 2);
+        const uint64_t dsf = make_smem_desc(base + kABytes + kBBytes, 128, 128, 0);
+        const uint32_t desc_a_lo = (uint32_t)dsw, desc_sw_hi = (uint32_t)(dsw >> 32);
+        const uint32_t desc_sf_lo = (uint32_t)dsf, desc_sf_hi = (uint32_t)(dsf >> 32);
+        const uint32_t full0 = smem_u32(&ctrl->full[0]);
+        const uint32_t empty0 = smem_u32(&ctrl->empty[0]);
+        int s = 0;
+        uint32_t ph = 0, acc_ph = 0;
+        bool ok = true;
+        int kcount = 0, tcount = 0;
+        for (int64_t tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+            if (!mbar_wait_warp(smem_u32(&ctrl->acc_empty), acc_ph ^ 1u, abort_flag, args.status, 2)) break;
+            if (lane == 0) TRACE(1024, tcount);
+            tcount++;
+            tc_fence_after();
+            for (int kb = 0; kb < num_kstages; kb++) {
+                if (!mbar_wait_warp(full0 + 8u * (uint32_t)s, ph, abort_flag, args.status, 3)) {
+                    ok = false;
+                    break;
+                }
+                if (lane == 0) TRACE(512, kcount);
                 tc_fence_after();
-                for (int kb = 0; kb < num_kstages; kb++) {
-                    if (!mbar_wait(smem_u32(&ctrl->full[s]), ph, abort_flag, args.status, 3)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t st = base + (uint32_t)(s * kStageBytes);
-                    const uint32_t sf_st = st + kABytes + kBBytes;
-                    const int nkk = min(4, num_kk - kb * 4);
+                // descriptors of this stage: only 32-bit adds in the loop
+                const uint32_t soff = (uint32_t)s * (kStageBytes >> 4);
+                const uint32_t a_lo = desc_a_lo + soff;
+                const uint32_t b_lo = a_lo + (kABytes >> 4);
+                const uint32_t f_lo = desc_sf_lo + soff;
+                const uint32_t sf_stage = tmem + kAccCols + (uint32_t)s * kSfColsPerStage;
+                const int nkk = min(4, num_kk - kb * 4);
+                const uint32_t acc0 = kb != 0 ? 1u : 0u;
+                if (nkk == 4) {
+                    // full stage: straight-line issue (no branches between
+                    // tcgen05 instructions keeps the tensor pipe fed)
+                    issue_sf4(sf_stage, f_lo, desc_sf_hi);
+                    mma_mxf4nvf4_warp(tmem, desc_from(a_lo, desc_sw_hi), desc_from(b_lo, desc_sw_hi), kIdesc,
+                                      sf_stage, sf_stage + 4, acc0);
+                    mma_mxf4nvf4_warp(tmem, desc_from(a_lo + 2u, desc_sw_hi), desc_from(b_lo + 2u, desc_sw_hi),
+                                      kIdesc, sf_stage + kSfColsPerKK, sf_stage + kSfColsPerKK + 4, 1u);
+                    mma_mxf4nvf4_warp(tmem, desc_from(a_lo + 4u, desc_sw_hi), desc_from(b_lo + 4u, desc_sw_hi),
+                                      kIdesc, sf_stage + 2 * kSfColsPerKK, sf_stage + 2 * kSfColsPerKK + 4, 1u);
+                    mma_mxf4nvf4_warp(tmem, desc_from(a_lo + 6u, desc_sw_hi), desc_from(b_lo + 6u, desc_sw_hi),
+                                      kIdesc, sf_stage + 3 * kSfColsPerKK, sf_stage + 3 * kSfColsPerKK + 4, 1u);
+                } else {
+                    // K tail: fewer than 4 K-steps
                     for (int kk = 0; kk < nkk; kk++) {
-                        const uint32_t sf_col = tmem + kAccCols + (uint32_t)s * kSfColsPerStage + (uint32_t)kk * kSfColsPerKK;
-                        tmem_copy_sf(sf_col, make_smem_desc(sf_st + kk * kSfTile, 128, 128, 0));
-                        tmem_copy_sf(sf_col + 4, make_smem_desc(sf_st + kSfaBytes + kk * kSfTile, 128, 128, 0));
-                        tmem_copy_sf(sf_col + 8, make_smem_desc(sf_st + kSfaBytes + (4 + kk) * kSfTile, 128, 128, 0));
-                        const uint64_t adesc = make_smem_desc(st + kk * 32, 16, 1024, 2);
-                        const uint64_t bdesc = make_smem_desc(st + kABytes + kk * 32, 16, 1024, 2);
-                        const uint32_t acc = (kb | kk) != 0 ? 1u : 0u;
-                        if (kMmaN == 256) {
-                            mma_mxf4nvf4(tmem, adesc, bdesc, kIdesc, sf_col, sf_col + 4, acc);
-                        } else {
-                            const uint64_t bdesc1 = make_smem_desc(st + kABytes + kBHalfBytes + kk * 32, 16, 1024, 2);
-                            mma_mxf4nvf4(tmem, adesc, bdesc, kIdesc, sf_col, sf_col + 4, acc);
-                            mma_mxf4nvf4(tmem + 128, adesc, bdesc1, kIdesc, sf_col, sf_col + 8, acc);
-                        }
+                        const uint32_t c = sf_stage + (uint32_t)kk * kSfColsPerKK;
+                        const uint32_t f = f_lo + (uint32_t)kk * (kSfTile >> 4);
+                        tmem_copy_sf_warp(c, desc_from(f, desc_sf_hi));
+                        tmem_copy_sf_warp(c + 4, desc_from(f + (kSfaBytes >> 4), desc_sf_hi));
+                        tmem_copy_sf_warp(c + 8, desc_from(f + ((kSfaBytes + 4 * kSfTile) >> 4), desc_sf_hi));
                     }
-                    mma_commit(smem_u32(&ctrl->empty[s]));
-                    if (++s == kStages) {
-                        s = 0;
-                        ph ^= 1u;
+                    for (int kk = 0; kk < nkk; kk++) {
+                        const uint32_t c = sf_stage + (uint32_t)kk * kSfColsPerKK;
+                        mma_mxf4nvf4_warp(tmem, desc_from(a_lo + 2u * kk, desc_sw_hi),
+                                          desc_from(b_lo + 2u * kk, desc_sw_hi), kIdesc, c, c + 4,
+                                          (kb | kk) != 0 ? 1u : 0u);
                     }
                 }
-                if (!ok) break;
-                mma_commit(smem_u32(&ctrl->acc_full));
-                acc_ph ^= 1u;
+                mma_commit_warp(empty0 + 8u * (uint32_t)s);
+                if (lane == 0) TRACE(768, kcount);
+                kcount++;
+                if (++s == kStages) {
+                    s = 0;
+                    ph ^= 1u;
+                }
             }
-            // every MMA this thread issued has completed before teardown
-            mma_commit(smem_u32(&ctrl->teardown));
-            const uint64_t t0 = globaltimer();
-            while (!mbar_try_wait(smem_u32(&ctrl->teardown), 0) && globaltimer() - t0 < kWaitLimitNs) {
-            }
+            if (!ok) break;
+            mma_commit_warp(smem_u32(&ctrl->acc_full));
+            acc_ph ^= 1u;
         }
+        // every MMA issued has completed before teardown
+        mma_commit_warp(smem_u32(&ctrl->teardown));
+        if (lane == 0) mbar_wait_teardown(smem_u32(&ctrl->teardown), 0);
+        __syncwarp();
     } else {
         // ------------------------------------------------------ epilogue
         const int q = warp & 3;             // tensor-memory lane quarter of this warp
@@ -258,14 +323,16 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         const float g_inter = args.epilogue == kEpiSwigluFp4 ? *args.g_inter : 1.0f;
         uint32_t acc_ph = 0;
         float wamax = 0.0f;
+        int ecount = 0;
         for (int64_t tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
             const int64_t mt = tile % num_m, nt = tile / num_m;
             // one lane waits; the warp then proceeds converged (tcgen05.ld is warp-wide)
             int ok = 1;
-            if (lane == 0) ok = mbar_wait(smem_u32(&ctrl->acc_full), acc_ph, abort_flag, args.status, 4) ? 1 : 0;
+            if (lane == 0) ok = mbar_wait<true>(smem_u32(&ctrl->acc_full), acc_ph, abort_flag, args.status, 4) ? 1 : 0;
             ok = __shfl_sync(0xffffffffu, ok, 0);
             __syncwarp();
             if (!ok) break;
+            if (warp == 2 && lane == 0) TRACE(1088, ecount);
             tc_fence_after();
             float v[128];
             if (!swiglu) {
@@ -283,6 +350,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&ctrl->acc_empty));
+            if (warp == 2 && lane == 0) TRACE(1152, ecount);
+            ecount++;
             acc_ph ^= 1u;
 
             const int64_t row = mt * 128 + q * 32 + lane;
@@ -409,3 +478,11 @@ cudaError_t launch_gemm(const CUtensorMap& map_a, const CUtensorMap& map_b0, con
 }
 
 }  // namespace nvfp4
+
+#ifdef NVFP4_TRACE
+extern "C" int nvfp4_debug_trace(unsigned long long* out, int n)
+{
+    if (n > 1216) n = 1216;
+    return cudaMemcpyFromSymbol(out, nvfp4::g_trace, n * sizeof(unsigned long long)) == cudaSuccess ? 0 : 4;
+}
+#endif

@@ -216,6 +216,36 @@ int nvfp4_mlp(const void* x, int64_t T, int64_t H, int64_t ldx,
               void* out, int64_t ldo, int add_residual,
               void* workspace, size_t workspace_bytes, nvfp4_stream_t stream);
 
+/*
+ * nvfp4_mlp_noalloc -- nvfp4_mlp for callers that cannot allocate device
+ * memory (no counterpart on the source pages; an addition of this library).
+ * Examples: a plugin that only receives borrowed tensor pointers from its host
+ * application and has no allocator, or a latency-critical caller for which
+ * cudaMalloc -- which may synchronise the whole device -- is not acceptable.
+ *
+ * Same computation, arguments, requirements and results as nvfp4_mlp, minus
+ * the workspace: the intermediates live in a fixed 32 MiB array inside this
+ * library (every GPU that loads the library holds it until the process
+ * exits).  A call whose nvfp4_mlp_workspace_bytes(T, H, I, inter_mode)
+ * exceeds 32 MiB returns NVFP4_ERR_WORKSPACE and enqueues nothing (at
+ * H=5120, I=17408 that allows T up to about 2500 tokens with
+ * NVFP4_INTER_STATIC and about 700 with NVFP4_INTER_DYNAMIC).
+ *   - Allocates nothing and calls no allocator.  It enqueues one small
+ *     cudaMemsetAsync that clears the array's amax words, then the
+ *     nvfp4_mlp launches.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current) and caches it; make that first call before any
+ *     stream capture.
+ *   - Every call shares the one array: calls that can overlap on the GPU
+ *     (different streams, or several host threads) race with each other and
+ *     must be serialised by the caller.
+ */
+int nvfp4_mlp_noalloc(const void* x, int64_t T, int64_t H, int64_t ldx,
+                      const void* norm_w, float eps,
+                      const nvfp4_tensor_t* W_gate, const nvfp4_tensor_t* W_up,
+                      const nvfp4_tensor_t* W_down, int inter_mode, float* g_inter,
+                      void* out, int64_t ldo, int add_residual, nvfp4_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

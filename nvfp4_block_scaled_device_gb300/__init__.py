@@ -60,6 +60,11 @@ _SIGS = {
                                  ctypes.POINTER(_TensorC), ctypes.POINTER(_TensorC), ctypes.c_int,
                                  ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int,
                                  ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    "nvfp4_mlp_noalloc": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                         ctypes.c_void_p, ctypes.c_float, ctypes.POINTER(_TensorC),
+                                         ctypes.POINTER(_TensorC), ctypes.POINTER(_TensorC), ctypes.c_int,
+                                         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int,
+                                         ctypes.c_void_p]),
 }
 
 EXPORTED_FUNCTIONS = tuple(_SIGS)
@@ -206,6 +211,19 @@ def nvfp4_gemm_swiglu(A: NVFP4Tensor, W_gate: NVFP4Tensor, W_up: NVFP4Tensor, in
     _check(lib().nvfp4_gemm_swiglu(ctypes.byref(a), ctypes.byref(wg), ctypes.byref(wu), inter_mode,
                                    _ptr(g_inter), _ptr(s_out.codes), s_out.codes.stride(0), _ptr(s_out.sf),
                                    _ptr(s_bf16), _ptr(ws), ws.numel(), _stream(stream)), "nvfp4_gemm_swiglu")
+
+
+def nvfp4_mlp_noalloc(x: torch.Tensor, norm_w: torch.Tensor, W_gate: NVFP4Tensor, W_up: NVFP4Tensor,
+                      W_down: NVFP4Tensor, inter_mode: int, g_inter: torch.Tensor, out: torch.Tensor,
+                      add_residual=True, eps=1e-6, stream=None):
+    """nvfp4_mlp without a workspace (the library's fixed scratch array; for
+    callers that cannot allocate device memory -- see include/nvfp4.h)."""
+    T, H, ldx = _bf16_2d(x, "x")
+    _, _, ldo = _bf16_2d(out, "out")
+    wg, wu, wd = W_gate.c(), W_up.c(), W_down.c()
+    _check(lib().nvfp4_mlp_noalloc(_ptr(x), T, H, ldx, _ptr(norm_w), eps, ctypes.byref(wg), ctypes.byref(wu),
+                                   ctypes.byref(wd), inter_mode, _ptr(g_inter), _ptr(out), ldo,
+                                   int(bool(add_residual)), _stream(stream)), "nvfp4_mlp_noalloc")
 
 
 def nvfp4_mlp(x: torch.Tensor, norm_w: torch.Tensor, W_gate: NVFP4Tensor, W_up: NVFP4Tensor,

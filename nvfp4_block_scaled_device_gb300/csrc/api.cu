@@ -154,7 +154,7 @@ int run_swiglu(const DeviceInfo* d, const nvfp4_tensor_t* A, const nvfp4_tensor_
         NVFP4_CUDA(launch_gemm(ma, mg, mu, a, d->num_sms, stream));
         NVFP4_CUDA(launch_finalize_scale(amax_ws, g_inter, stream));
         NVFP4_CUDA(launch_quantize(s_bf16, T, I, I, nullptr, 0.0f, g_inter, s_codes, ld_s_codes, s_sf, nullptr,
-                                   stream));
+                                   d->num_sms, stream));
     }
     return NVFP4_OK;
 }
@@ -267,7 +267,7 @@ int nvfp4_quantize(const void* x, int64_t rows, int64_t cols, int64_t ldx, const
     NVFP4_TRY(device_info(&d));
     NVFP4_CUDA(launch_quantize(static_cast<const __nv_bfloat16*>(x), rows, cols, ldx,
                                static_cast<const __nv_bfloat16*>(norm_w), eps, g, codes, ld_codes, sf,
-                               static_cast<__nv_bfloat16*>(y_out), (cudaStream_t)stream));
+                               static_cast<__nv_bfloat16*>(y_out), d->num_sms, (cudaStream_t)stream));
     return NVFP4_OK;
 }
 
@@ -367,7 +367,7 @@ int nvfp4_mlp(const void* x, int64_t T, int64_t H, int64_t ldx, const void* norm
     const __nv_bfloat16* nw = static_cast<const __nv_bfloat16*>(norm_w);
     // 1-2: RMSNorm prologue -> device scale -> FP4 input
     NVFP4_CUDA(launch_amax_scale(xb, T, H, ldx, nw, eps, g_h, amax_ws, d->num_sms, st));
-    NVFP4_CUDA(launch_quantize(xb, T, H, ldx, nw, eps, g_h, h_codes, H / 2, h_sf, nullptr, st));
+    NVFP4_CUDA(launch_quantize(xb, T, H, ldx, nw, eps, g_h, h_codes, H / 2, h_sf, nullptr, d->num_sms, st));
     // 3: fused gate/up GEMM + SwiGLU + FP4 requant
     const nvfp4_tensor_t h = {h_codes, h_sf, g_h, T, H, H / 2};
     NVFP4_TRY(run_swiglu(d, &h, W_gate, W_up, inter_mode, g_inter, s_codes, I / 2, s_sf, nullptr, swiglu_ws, st));

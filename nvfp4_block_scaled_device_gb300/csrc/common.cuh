@@ -405,10 +405,27 @@ __device__ __forceinline__ int64_t sf_offset(int64_t r, int64_t c, int64_t kb_pa
     return ((r >> 7) * (kb_pad >> 2) + (c >> 2)) * 512 + (r & 31) * 16 + ((r & 127) >> 5) * 4 + (c & 3);
 }
 
+// Correctly rounded binary32 quotient a / b for many a and one b > 0
+// (normal, with a / b far from overflow and underflow), from the correctly
+// rounded reciprocal y = RN(1/b): q0 = RN(a*y), the remainder
+// r = a - b*q0 is exact in one FMA, and RN(q0 + r*y) = RN(a/b)
+// (P. Markstein, "Computation of elementary functions on the IBM RISC
+// System/6000 processor", IBM J. Res. Dev. 34(1), 1990: quotient refinement
+// with a correctly rounded reciprocal).
+__device__ __forceinline__ float div_by_recip(float a, float b, float y)
+{
+    const float q0 = __fmul_rn(a, y);
+    const float r = __fmaf_rn(-q0, b, a);
+    // b > 0: the quotient has a's sign; this also keeps -0 / b = -0
+    return copysignf(__fmaf_rn(r, y, q0), a);
+}
+
 // Quantize one 16-element block held as two halves of 8 in lanes l, l^1:
 // shared helper so every kernel takes bit-identical decisions.
 //   v: this lane's 8 values; g: global scale.  Returns this lane's 8 codes
 //   (32 bits) and writes the block's scale byte to *sc.
+// Arithmetic (binary32, one rounding per step): d = 6*g, s = E4M3(amax16/d),
+// den = E4M3val(s)*g, code_i = E2M1(v_i/den).
 __device__ __forceinline__ uint32_t quant_half_block(const float* v, float g, float amax16, uint32_t* sc_out)
 {
     const float d = __fmul_rn(6.0f, g);
@@ -417,9 +434,10 @@ __device__ __forceinline__ uint32_t quant_half_block(const float* v, float g, fl
     *sc_out = sc;
     if (sc == 0) return 0u;
     const float den = __fmul_rn(e4m3_to_f32(sc), g);
+    const float y = __frcp_rn(den);
     float q[8];
 #pragma unroll
-    for (int i = 0; i < 8; i++) q[i] = __fdiv_rn(v[i], den);
+    for (int i = 0; i < 8; i++) q[i] = div_by_recip(v[i], den, y);
     return cvt_e2m1x8(q);
 }
 

@@ -22,7 +22,8 @@ cudaError_t launch_amax_scale(const __nv_bfloat16* x, int64_t rows, int64_t cols
 
 cudaError_t launch_quantize(const __nv_bfloat16* x, int64_t rows, int64_t cols, int64_t ldx,
                             const __nv_bfloat16* norm_w, float eps, const float* g, uint8_t* codes,
-                            int64_t ld_codes, uint8_t* sf, __nv_bfloat16* y_out, cudaStream_t stream);
+                            int64_t ld_codes, uint8_t* sf, __nv_bfloat16* y_out, int num_sms,
+                            cudaStream_t stream);
 
 // g_out = max(amax(ws), 1e-8) / 2688, and the amax word is reset to zero.
 cudaError_t launch_finalize_scale(uint32_t* ws, float* g_out, cudaStream_t stream);

@@ -94,7 +94,7 @@ def recorded_traffic():
 
 def kernel_source_hash():
     h = hashlib.sha256()
-    for f in ("gemm.cu", "common.cuh", "internal.h"):
+    for f in ("gemm.cu", "gemm2.cu", "gemm_epilogue.cuh", "common.cuh", "internal.h"):
         h.update(open(os.path.join(ROOT, "nvfp4_block_scaled_device_gb300", "csrc", f), "rb").read())
     return h.hexdigest()[:16]
 

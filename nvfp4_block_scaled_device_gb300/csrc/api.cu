@@ -64,12 +64,13 @@ int encoder()
     return NVFP4_OK;
 }
 
-// 2-D byte tensor [rows x row_bytes], pitch ld, 128x128-byte boxes, 128-B swizzle.
+// 2-D byte tensor [rows x row_bytes], pitch ld, boxes of 128 bytes x
+// kCodeBoxRows rows, 128-B swizzle.
 int make_codes_map(CUtensorMap* m, const void* base, int64_t rows, int64_t row_bytes, int64_t ld)
 {
     cuuint64_t dims[2] = {(cuuint64_t)row_bytes, (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)ld};
-    cuuint32_t box[2] = {128, 128};
+    cuuint32_t box[2] = {128, (cuuint32_t)nvfp4::kCodeBoxRows};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -111,6 +112,18 @@ int64_t sf_tile_stride(int64_t cols) { return pad_to(cols / 16, 4) / 4 * 512; }
         if ((expr) != cudaSuccess) return NVFP4_ERR_CUDA; \
     } while (0)
 
+// The SM-pair kernel (256-row tiles) takes M >= kPairMinRows; below that,
+// one 128-row tile per CTA.  The pair kernel currently measures slower than
+// the 1-SM kernel at every block shape, so the threshold is set above any M.
+constexpr int64_t kPairMinRows = INT64_MAX;
+
+cudaError_t run_gemm(const CUtensorMap& ma, const CUtensorMap& mb0, const CUtensorMap& mb1, const GemmArgs& a,
+                     const DeviceInfo* d, cudaStream_t stream)
+{
+    if (a.M >= kPairMinRows) return launch_gemm2(ma, mb0, mb1, a, d->num_sms, stream);
+    return launch_gemm(ma, mb0, mb1, a, d->num_sms, stream);
+}
+
 // Shared by nvfp4_gemm_swiglu and nvfp4_mlp.
 int run_swiglu(const DeviceInfo* d, const nvfp4_tensor_t* A, const nvfp4_tensor_t* Wg, const nvfp4_tensor_t* Wu,
                int mode, float* g_inter, uint8_t* s_codes, int64_t ld_s_codes, uint8_t* s_sf,
@@ -144,14 +157,14 @@ int run_swiglu(const DeviceInfo* d, const nvfp4_tensor_t* A, const nvfp4_tensor_
         a.g_inter = g_inter;
         a.s_bf16 = s_bf16_user;
         a.ld_s = I;
-        NVFP4_CUDA(launch_gemm(ma, mg, mu, a, d->num_sms, stream));
+        NVFP4_CUDA(run_gemm(ma, mg, mu, a, d, stream));
     } else {
         __nv_bfloat16* s_bf16 = s_bf16_user ? s_bf16_user : reinterpret_cast<__nv_bfloat16*>(ws + 256);
         a.epilogue = kEpiSwigluBf16;
         a.s_bf16 = s_bf16;
         a.ld_s = I;
         a.amax_ws = amax_ws;
-        NVFP4_CUDA(launch_gemm(ma, mg, mu, a, d->num_sms, stream));
+        NVFP4_CUDA(run_gemm(ma, mg, mu, a, d, stream));
         NVFP4_CUDA(launch_finalize_scale(amax_ws, g_inter, stream));
         NVFP4_CUDA(launch_quantize(s_bf16, T, I, I, nullptr, 0.0f, g_inter, s_codes, ld_s_codes, s_sf, nullptr,
                                    d->num_sms, stream));
@@ -301,7 +314,7 @@ int nvfp4_gemm(const nvfp4_tensor_t* A, const nvfp4_tensor_t* W, void* out, int6
     a.residual = static_cast<const __nv_bfloat16*>(residual);
     a.ldr = ldr;
     a.status = d->status;
-    NVFP4_CUDA(launch_gemm(ma, mb, mb, a, d->num_sms, (cudaStream_t)stream));
+    NVFP4_CUDA(run_gemm(ma, mb, mb, a, d, (cudaStream_t)stream));
     return NVFP4_OK;
 }
 
@@ -392,7 +405,7 @@ int nvfp4_mlp(const void* x, int64_t T, int64_t H, int64_t ldx, const void* norm
     a.residual = add_residual ? xb : nullptr;
     a.ldr = ldx;
     a.status = d->status;
-    NVFP4_CUDA(launch_gemm(ma, mb, mb, a, d->num_sms, st));
+    NVFP4_CUDA(run_gemm(ma, mb, mb, a, d, st));
     return NVFP4_OK;
 }
 

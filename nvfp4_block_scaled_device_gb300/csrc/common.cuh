@@ -122,6 +122,21 @@ __device__ __forceinline__ void mbar_wait_teardown(uint32_t bar, uint32_t parity
     }
 }
 
+// Per-warpgroup register budget (all four warps of a warpgroup execute the
+// same instruction).  The block's registers are split per SM sub-partition,
+// one warp of each warpgroup per sub-partition: the decreases must free what
+// the increases take.
+template <uint32_t kRegs>
+__device__ __forceinline__ void setmaxnreg_dec()
+{
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+template <uint32_t kRegs>
+__device__ __forceinline__ void setmaxnreg_inc()
+{
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+
 // ------------------------------------------------------------------ TMA
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
                                             int32_t x, int32_t y, uint64_t cache_hint)
@@ -347,6 +362,142 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v)
 __device__ __forceinline__ void tmem_ld_wait()
 {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// ------------------------------------------------------- clusters (2-SM)
+__device__ __forceinline__ uint32_t cluster_ctarank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Address of the same shared-memory offset in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_to_cta(uint32_t addr, uint32_t rank)
+{
+    uint32_t out;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(out) : "r"(addr), "r"(rank));
+    return out;
+}
+
+__device__ __forceinline__ void cluster_sync_all()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Arrive on an mbarrier of another CTA of the cluster (cluster-scope release).
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr)
+{
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+// try_wait with cluster-scope acquire; with kSleep the thread may suspend
+// (no issue slots used) until the phase completes or about 20 us pass.
+template <bool kSleep>
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    if (kSleep)
+        asm volatile(
+            "{\n .reg .pred p;\n"
+            " mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n"
+            " selp.u32 %0, 1, 0, p;\n}"
+            : "=r"(ok)
+            : "r"(bar), "r"(parity), "r"(20000u)
+            : "memory");
+    else
+        asm volatile(
+            "{\n .reg .pred p;\n"
+            " mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+            " selp.u32 %0, 1, 0, p;\n}"
+            : "=r"(ok)
+            : "r"(bar), "r"(parity)
+            : "memory");
+    return ok != 0;
+}
+
+// Warp-wide bounded wait with cluster-scope acquire (for phases completed
+// by the other CTA of the pair): lane 0 polls, the result is broadcast and
+// the warp leaves converged.
+template <bool kSleep = false>
+__device__ __forceinline__ bool mbar_wait_cluster_warp(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                                       int* status, int site)
+{
+    int ok = 1;
+    if ((threadIdx.x & 31) == 0) {
+        ok = 0;
+        const uint64_t t0 = clock64();
+        for (uint32_t i = 0;; i++) {
+            if (mbar_try_wait_cluster<kSleep>(bar, parity)) {
+                ok = 1;
+                break;
+            }
+            if ((i & 63u) == 63u) {
+                if (*abort_flag) break;
+                if ((uint64_t)(clock64() - t0) > kWaitLimitCycles) {
+                    *abort_flag = 1;
+                    if (status) atomicCAS(status, 0, kErrTimeout * 100 + site);
+                    break;
+                }
+            }
+        }
+    }
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    __syncwarp();
+    return ok != 0;
+}
+
+// 2-SM (cta_group::2) tensor-core operations: issued by the pair's even CTA
+// for both CTAs; operands sit at the same shared/tensor-memory addresses in
+// both.  The whole (converged) warp executes these; one lane issues.
+__device__ __forceinline__ void tmem_alloc2(uint32_t dst_smem, uint32_t ncols)
+{
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish2()
+{
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc2(uint32_t taddr, uint32_t ncols)
+{
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ void mma2_mxf4nvf4_warp(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                                   uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n .reg .pred p, e;\n .reg .b32 r;\n"
+        " setp.ne.b32 p, %6, 0;\n"
+        " elect.sync r|e, 0xffffffff;\n"
+        " @e tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n"
+        "}\n" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_copy_sf2_warp(uint32_t taddr, uint64_t src_desc)
+{
+    asm volatile(
+        "{\n .reg .pred e;\n .reg .b32 r;\n elect.sync r|e, 0xffffffff;\n"
+        " @e tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;\n}" ::"r"(taddr),
+        "l"(src_desc)
+        : "memory");
+}
+
+// Arrive on the mbarrier at offset `bar` of every CTA in `cta_mask` once all
+// 2-SM tensor-core operations issued so far have completed.
+__device__ __forceinline__ void mma_commit2_mc_warp(uint32_t bar, uint16_t cta_mask)
+{
+    asm volatile(
+        "{\n .reg .pred e;\n .reg .b32 r;\n elect.sync r|e, 0xffffffff;\n"
+        " @e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;\n}" ::"r"(
+            bar),
+        "h"(cta_mask)
+        : "memory");
 }
 
 // ---------------------------------------------------- FP4 / FP8 convert

@@ -13,6 +13,13 @@ namespace nvfp4 {
 // RMSNorm they compute is bit-identical.
 constexpr int kRowThreads = 256;
 
+// Rows per TMA box of the FP4 code tensors (128 bytes wide, 128-byte
+// swizzle).  A 128-row operand tile is fetched as two boxes, issued by two
+// different threads: the copies one thread issues are served one after the
+// other (about 25 bytes per clock each), so a stage's copies are spread over
+// several issuing lanes.
+constexpr int kCodeBoxRows = 64;
+
 // Workspace words used by the amax reduction: [0] amax bits, [1] ticket.
 constexpr size_t kAmaxWorkspaceBytes = 8;
 
@@ -67,6 +74,11 @@ struct GemmArgs {
 // box and 128-byte swizzle.
 cudaError_t launch_gemm(const CUtensorMap& map_a, const CUtensorMap& map_b0, const CUtensorMap& map_b1,
                         const GemmArgs& args, int num_sms, cudaStream_t stream);
+
+// 2-SM version (clusters of 2 CTAs, 256-row tiles): same arguments and
+// results; used for M > 128.
+cudaError_t launch_gemm2(const CUtensorMap& map_a, const CUtensorMap& map_b0, const CUtensorMap& map_b1,
+                         const GemmArgs& args, int num_sms, cudaStream_t stream);
 
 size_t gemm_smem_bytes();
 

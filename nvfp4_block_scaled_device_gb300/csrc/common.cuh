@@ -321,12 +321,61 @@ __device__ __forceinline__ void bulk_load_warp(uint32_t dst, const void* src, ui
         : "memory");
 }
 
-// Warp-wide bounded wait: lane 0 polls, the result is broadcast and the
-// warp leaves converged.
+// Converged fast path of a warp-wide wait: every lane polls, a vote makes
+// the outcome warp-uniform, and the loop stays inside one asm block, so a
+// warp issuing tensor-core instructions meets no divergent branch.  Gives up
+// (returns false) after kFastPolls incomplete polls.
+constexpr uint32_t kFastPolls = 256;
+
+__device__ __forceinline__ bool mbar_poll_warp(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p, q;\n .reg .u32 n;\n mov.u32 n, 0;\n"
+        "POLL_%=:\n"
+        " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " vote.sync.all.pred p, p, 0xffffffff;\n"
+        " @p bra.uni DONE_%=;\n"
+        " add.u32 n, n, 1;\n"
+        " setp.lt.u32 q, n, %3;\n"
+        " @q bra.uni POLL_%=;\n"
+        "DONE_%=:\n"
+        " selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "n"(kFastPolls)
+        : "memory");
+    return ok != 0;
+}
+
+// As mbar_poll_warp, with cluster-scope acquire.
+__device__ __forceinline__ bool mbar_poll_cluster_warp(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p, q;\n .reg .u32 n;\n mov.u32 n, 0;\n"
+        "POLL_%=:\n"
+        " mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+        " vote.sync.all.pred p, p, 0xffffffff;\n"
+        " @p bra.uni DONE_%=;\n"
+        " add.u32 n, n, 1;\n"
+        " setp.lt.u32 q, n, %3;\n"
+        " @q bra.uni POLL_%=;\n"
+        "DONE_%=:\n"
+        " selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "n"(kFastPolls)
+        : "memory");
+    return ok != 0;
+}
+
+// Warp-wide bounded wait: the converged fast path first; if the phase is
+// still incomplete, lane 0 keeps polling (bounded, see mbar_wait), the
+// result is broadcast and the warp leaves converged.
 template <bool kSleep = false>
 __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* status,
                                                int site)
 {
+    if (!kSleep && mbar_poll_warp(bar, parity)) return true;
     int ok = 1;
     if ((threadIdx.x & 31) == 0) ok = mbar_wait<kSleep>(bar, parity, abort_flag, status, site) ? 1 : 0;
     ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -417,12 +466,13 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
 }
 
 // Warp-wide bounded wait with cluster-scope acquire (for phases completed
-// by the other CTA of the pair): lane 0 polls, the result is broadcast and
-// the warp leaves converged.
+// by the other CTA of the pair): the converged fast path first, then lane 0
+// polls, the result is broadcast and the warp leaves converged.
 template <bool kSleep = false>
 __device__ __forceinline__ bool mbar_wait_cluster_warp(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                                        int* status, int site)
 {
+    if (!kSleep && mbar_poll_cluster_warp(bar, parity)) return true;
     int ok = 1;
     if ((threadIdx.x & 31) == 0) {
         ok = 0;
@@ -497,6 +547,134 @@ __device__ __forceinline__ void mma_commit2_mc_warp(uint32_t bar, uint16_t cta_m
         " @e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;\n}" ::"r"(
             bar),
         "h"(cta_mask)
+        : "memory");
+}
+
+// ------------------------------------------------- fused stage issue
+// One full K stage (4 K-steps of 64): its 12 scale-tile copies shared ->
+// tensor memory (A, B rows 0-127, B rows 128-255 per K-step), its 4 MMAs
+// and the commit that frees the stage, all from one asm block with a single
+// elect.sync.  The warp stays converged from the first instruction to the
+// last: issuing each tensor-core instruction from its own elected block, or
+// any branch between them, slows the tensor pipe's intake.
+//   acc: accumulator (tensor memory)     sfc: this stage's first scale column
+//   f_lo / sf_hi: scale-tile descriptor of the stage (16-byte units in lo)
+//   a_lo / b_lo / sw_hi: A and B code descriptors of the stage
+//   acc0: accumulate into acc for the first K-step (0 = overwrite)
+//   bar: mbarrier the commit arrives on
+// Layout assumed: scale tiles of one K-step 512 B apart, the B tiles at
+// +2048 and +4096 bytes; code K-steps 32 bytes apart; scale columns per
+// K-step: A at +0, B rows 0-127 at +4, B rows 128-255 at +8, 12 per K-step.
+__device__ __forceinline__ void stage_issue_1sm(uint32_t acc, uint32_t sfc, uint32_t f_lo, uint32_t sf_hi,
+                                                uint32_t a_lo, uint32_t b_lo, uint32_t sw_hi, uint32_t idesc,
+                                                uint32_t acc0, uint32_t bar)
+{
+    asm volatile(
+        "{\n"
+        " .reg .pred e, p, pt;\n"
+        " .reg .b32 r, t, lo;\n"
+        " .reg .b64 d, da, db;\n"
+        " elect.sync r|e, 0xffffffff;\n"
+        " setp.ne.b32 p, %8, 0;\n"
+        " setp.eq.b32 pt, 0, 0;\n"
+        " add.u32 t, %1, 0; add.u32 lo, %2, 0; mov.b64 d, {lo, %3};\n"
+        " @e tcgen05.cp.cta_group::1.32x128b.warpx4 [t], d;\n"
+        " add.u32 t, %1, 4; add.u32 lo, %2, 128; mov.b64 d, {lo, %3};\n"
+        " @e tcgen05.cp.cta_group::1.32x128b.warpx4 [t], d;\n"
+        " add.u32 t, %1, 8; add.u32 lo, %2, 256; mov.b64 d, {lo, %3};\n"
+        " @e tcgen05.cp.cta_group::1.32x128b.warpx4 [t], d;\n"
+        " add.u32 t, %1, 12; add.u32 lo, %2, 32; mov.b64 d, {lo, %3};\n"
+        " @e tcgen05.cp.cta_group::1.32x128b.warpx4 [t], d;\n"
+        " add.u32 t, %1, 16; add.u32 lo, %2, 160; mov.b64 d, {lo, %3};\n"
+        " @e tcgen05.cp.cta_group::1.32x128b.warpx4 [t], d;\n"
+        " add.u32 t, %1, 20; add.u32 lo, %2, 288; mov.b64 d, {lo, %3};\n"
+        " @e tcgen05.cp.cta_group::1.32x128b.warpx4 [t], d;\n"
+        " add.u32 t, %1, 24; add.u32 lo, %2, 64; mov.b64 d, {lo, %3};\n"
+        " @e tcgen05.cp.cta_group::1.32x128b.warpx4 [t], d;\n"
+        " add.u32 t, %1, 28; add.u32 lo, %2, 192; mov.b64 d, {lo, %3};\n"
+        " @e tcgen05.cp.cta_group::1.32x128b.warpx4 [t], d;\n"
+        " add.u32 t, %1, 32; add.u32 lo, %2, 320; mov.b64 d, {lo, %3};\n"
+        " @e tcgen05.cp.cta_group::1.32x128b.warpx4 [t], d;\n"
+        " add.u32 t, %1, 36; add.u32 lo, %2, 96; mov.b64 d, {lo, %3};\n"
+        " @e tcgen05.cp.cta_group::1.32x128b.warpx4 [t], d;\n"
+        " add.u32 t, %1, 40; add.u32 lo, %2, 224; mov.b64 d, {lo, %3};\n"
+        " @e tcgen05.cp.cta_group::1.32x128b.warpx4 [t], d;\n"
+        " add.u32 t, %1, 44; add.u32 lo, %2, 352; mov.b64 d, {lo, %3};\n"
+        " @e tcgen05.cp.cta_group::1.32x128b.warpx4 [t], d;\n"
+        " add.u32 lo, %4, 0; mov.b64 da, {lo, %6}; add.u32 lo, %5, 0; mov.b64 db, {lo, %6};\n"
+        " add.u32 t, %1, 0; add.u32 r, %1, 4;\n"
+        " @e tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], da, db, %7, [t], [r], p;\n"
+        " add.u32 lo, %4, 2; mov.b64 da, {lo, %6}; add.u32 lo, %5, 2; mov.b64 db, {lo, %6};\n"
+        " add.u32 t, %1, 12; add.u32 r, %1, 16;\n"
+        " @e tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], da, db, %7, [t], [r], pt;\n"
+        " add.u32 lo, %4, 4; mov.b64 da, {lo, %6}; add.u32 lo, %5, 4; mov.b64 db, {lo, %6};\n"
+        " add.u32 t, %1, 24; add.u32 r, %1, 28;\n"
+        " @e tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], da, db, %7, [t], [r], pt;\n"
+        " add.u32 lo, %4, 6; mov.b64 da, {lo, %6}; add.u32 lo, %5, 6; mov.b64 db, {lo, %6};\n"
+        " add.u32 t, %1, 36; add.u32 r, %1, 40;\n"
+        " @e tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], da, db, %7, [t], [r], pt;\n"
+        " @e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%9];\n"
+        "}\n"
+        ::"r"(acc), "r"(sfc), "r"(f_lo), "r"(sf_hi), "r"(a_lo), "r"(b_lo), "r"(sw_hi), "r"(idesc), "r"(acc0),
+        "r"(bar)
+        : "memory");
+}
+
+// The same for an SM pair (cta_group::2): the copies and MMAs act on both
+// CTAs' shared and tensor memory, and the commit arrives on `bar` in every
+// CTA of `cta_mask`.
+__device__ __forceinline__ void stage_issue_2sm(uint32_t acc, uint32_t sfc, uint32_t f_lo, uint32_t sf_hi,
+                                                uint32_t a_lo, uint32_t b_lo, uint32_t sw_hi, uint32_t idesc,
+                                                uint32_t acc0, uint32_t bar, uint16_t cta_mask)
+{
+    asm volatile(
+        "{\n"
+        " .reg .pred e, p, pt;\n"
+        " .reg .b32 r, t, lo;\n"
+        " .reg .b64 d, da, db;\n"
+        " elect.sync r|e, 0xffffffff;\n"
+        " setp.ne.b32 p, %8, 0;\n"
+        " setp.eq.b32 pt, 0, 0;\n"
+        " add.u32 t, %1, 0; add.u32 lo, %2, 0; mov.b64 d, {lo, %3};\n"
+        " @e tcgen05.cp.cta_group::2.32x128b.warpx4 [t], d;\n"
+        " add.u32 t, %1, 4; add.u32 lo, %2, 128; mov.b64 d, {lo, %3};\n"
+        " @e tcgen05.cp.cta_group::2.32x128b.warpx4 [t], d;\n"
+        " add.u32 t, %1, 8; add.u32 lo, %2, 256; mov.b64 d, {lo, %3};\n"
+        " @e tcgen05.cp.cta_group::2.32x128b.warpx4 [t], d;\n"
+        " add.u32 t, %1, 12; add.u32 lo, %2, 32; mov.b64 d, {lo, %3};\n"
+        " @e tcgen05.cp.cta_group::2.32x128b.warpx4 [t], d;\n"
+        " add.u32 t, %1, 16; add.u32 lo, %2, 160; mov.b64 d, {lo, %3};\n"
+        " @e tcgen05.cp.cta_group::2.32x128b.warpx4 [t], d;\n"
+        " add.u32 t, %1, 20; add.u32 lo, %2, 288; mov.b64 d, {lo, %3};\n"
+        " @e tcgen05.cp.cta_group::2.32x128b.warpx4 [t], d;\n"
+        " add.u32 t, %1, 24; add.u32 lo, %2, 64; mov.b64 d, {lo, %3};\n"
+        " @e tcgen05.cp.cta_group::2.32x128b.warpx4 [t], d;\n"
+        " add.u32 t, %1, 28; add.u32 lo, %2, 192; mov.b64 d, {lo, %3};\n"
+        " @e tcgen05.cp.cta_group::2.32x128b.warpx4 [t], d;\n"
+        " add.u32 t, %1, 32; add.u32 lo, %2, 320; mov.b64 d, {lo, %3};\n"
+        " @e tcgen05.cp.cta_group::2.32x128b.warpx4 [t], d;\n"
+        " add.u32 t, %1, 36; add.u32 lo, %2, 96; mov.b64 d, {lo, %3};\n"
+        " @e tcgen05.cp.cta_group::2.32x128b.warpx4 [t], d;\n"
+        " add.u32 t, %1, 40; add.u32 lo, %2, 224; mov.b64 d, {lo, %3};\n"
+        " @e tcgen05.cp.cta_group::2.32x128b.warpx4 [t], d;\n"
+        " add.u32 t, %1, 44; add.u32 lo, %2, 352; mov.b64 d, {lo, %3};\n"
+        " @e tcgen05.cp.cta_group::2.32x128b.warpx4 [t], d;\n"
+        " add.u32 lo, %4, 0; mov.b64 da, {lo, %6}; add.u32 lo, %5, 0; mov.b64 db, {lo, %6};\n"
+        " add.u32 t, %1, 0; add.u32 r, %1, 4;\n"
+        " @e tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], da, db, %7, [t], [r], p;\n"
+        " add.u32 lo, %4, 2; mov.b64 da, {lo, %6}; add.u32 lo, %5, 2; mov.b64 db, {lo, %6};\n"
+        " add.u32 t, %1, 12; add.u32 r, %1, 16;\n"
+        " @e tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], da, db, %7, [t], [r], pt;\n"
+        " add.u32 lo, %4, 4; mov.b64 da, {lo, %6}; add.u32 lo, %5, 4; mov.b64 db, {lo, %6};\n"
+        " add.u32 t, %1, 24; add.u32 r, %1, 28;\n"
+        " @e tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], da, db, %7, [t], [r], pt;\n"
+        " add.u32 lo, %4, 6; mov.b64 da, {lo, %6}; add.u32 lo, %5, 6; mov.b64 db, {lo, %6};\n"
+        " add.u32 t, %1, 36; add.u32 r, %1, 40;\n"
+        " @e tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], da, db, %7, [t], [r], pt;\n"
+        " @e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%9], %10;\n"
+        "}\n"
+        ::"r"(acc), "r"(sfc), "r"(f_lo), "r"(sf_hi), "r"(a_lo), "r"(b_lo), "r"(sw_hi), "r"(idesc), "r"(acc0),
+        "r"(bar), "h"(cta_mask)
         : "memory");
 }
 

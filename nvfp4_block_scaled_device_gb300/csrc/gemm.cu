@@ -92,25 +92,6 @@ struct Ctrl {
 };
 static_assert(sizeof(Ctrl) <= kCtrlBytes, "control block");
 
-// The 12 scale-tile copies of a full stage (A, B rows 0-127, B rows
-// 128-255, for each of 4 K-steps), straight-line.
-__device__ __forceinline__ void issue_sf4(uint32_t c, uint32_t f, uint32_t hi)
-{
-    constexpr uint32_t kB0 = kSfaBytes >> 4, kB1 = (kSfaBytes + 4 * kSfTile) >> 4, kT = kSfTile >> 4;
-    tmem_copy_sf_warp(c, desc_from(f, hi));
-    tmem_copy_sf_warp(c + 4, desc_from(f + kB0, hi));
-    tmem_copy_sf_warp(c + 8, desc_from(f + kB1, hi));
-    tmem_copy_sf_warp(c + kSfColsPerKK, desc_from(f + kT, hi));
-    tmem_copy_sf_warp(c + kSfColsPerKK + 4, desc_from(f + kT + kB0, hi));
-    tmem_copy_sf_warp(c + kSfColsPerKK + 8, desc_from(f + kT + kB1, hi));
-    tmem_copy_sf_warp(c + 2 * kSfColsPerKK, desc_from(f + 2 * kT, hi));
-    tmem_copy_sf_warp(c + 2 * kSfColsPerKK + 4, desc_from(f + 2 * kT + kB0, hi));
-    tmem_copy_sf_warp(c + 2 * kSfColsPerKK + 8, desc_from(f + 2 * kT + kB1, hi));
-    tmem_copy_sf_warp(c + 3 * kSfColsPerKK, desc_from(f + 3 * kT, hi));
-    tmem_copy_sf_warp(c + 3 * kSfColsPerKK + 4, desc_from(f + 3 * kT + kB0, hi));
-    tmem_copy_sf_warp(c + 3 * kSfColsPerKK + 8, desc_from(f + 3 * kT + kB1, hi));
-}
-
 __global__ void __launch_bounds__(kNumThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b0,
                 const __grid_constant__ CUtensorMap map_b1, const GemmArgs args)
@@ -131,6 +112,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     const int64_t num_tiles = num_m * num_n;
     const int num_kk = (int)(args.K / 64);
     const int num_kstages = (num_kk + 3) / 4;
+    const int full_kstages = num_kk / 4;       // stages of 4 K-steps
+    const int tail_kk = num_kk % 4;            // K-steps of a last, partial stage
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; s++) {
@@ -268,58 +251,60 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             int kcount = 0, tcount = 0;
             for (int64_t tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
                 if (!mbar_wait_warp(smem_u32(&ctrl->acc_empty), acc_ph ^ 1u, abort_flag, args.status, 2)) break;
-                if (lane == 0) TRACE(1024, tcount);
+                TRACE(1024, tcount);
                 tcount++;
                 tc_fence_after();
-                for (int kb = 0; kb < num_kstages; kb++) {
+                // full stages: nothing but the wait and one fused issue block
+                for (int kb = 0; kb < full_kstages; kb++) {
                     if (!mbar_wait_warp(full0 + 8u * (uint32_t)s, ph, abort_flag, args.status, 3)) {
                         ok = false;
                         break;
                     }
-                    if (lane == 0) TRACE(512, kcount);
+                    TRACE(512, kcount);
                     tc_fence_after();
                     // descriptors of this stage: only 32-bit adds in the loop
                     const uint32_t soff = (uint32_t)s * (kStageBytes >> 4);
                     const uint32_t a_lo = desc_a_lo + soff;
-                    const uint32_t b_lo = a_lo + (kABytes >> 4);
-                    const uint32_t f_lo = desc_sf_lo + soff;
-                    const uint32_t sf_stage = tmem + kAccCols + (uint32_t)s * kSfColsPerStage;
-                    const int nkk = min(4, num_kk - kb * 4);
-                    const uint32_t acc0 = kb != 0 ? 1u : 0u;
-                    if (nkk == 4) {
-                        // full stage: straight-line issue (no branches between
-                        // tcgen05 instructions keeps the tensor pipe fed)
-                        issue_sf4(sf_stage, f_lo, desc_sf_hi);
-                        mma_mxf4nvf4_warp(tmem, desc_from(a_lo, desc_sw_hi), desc_from(b_lo, desc_sw_hi), kIdesc,
-                                          sf_stage, sf_stage + 4, acc0);
-                        mma_mxf4nvf4_warp(tmem, desc_from(a_lo + 2u, desc_sw_hi), desc_from(b_lo + 2u, desc_sw_hi),
-                                          kIdesc, sf_stage + kSfColsPerKK, sf_stage + kSfColsPerKK + 4, 1u);
-                        mma_mxf4nvf4_warp(tmem, desc_from(a_lo + 4u, desc_sw_hi), desc_from(b_lo + 4u, desc_sw_hi),
-                                          kIdesc, sf_stage + 2 * kSfColsPerKK, sf_stage + 2 * kSfColsPerKK + 4, 1u);
-                        mma_mxf4nvf4_warp(tmem, desc_from(a_lo + 6u, desc_sw_hi), desc_from(b_lo + 6u, desc_sw_hi),
-                                          kIdesc, sf_stage + 3 * kSfColsPerKK, sf_stage + 3 * kSfColsPerKK + 4, 1u);
+                    stage_issue_1sm(tmem, tmem + kAccCols + (uint32_t)s * kSfColsPerStage, desc_sf_lo + soff,
+                                    desc_sf_hi, a_lo, a_lo + (kABytes >> 4), desc_sw_hi, kIdesc, kb != 0 ? 1u : 0u,
+                                    empty0 + 8u * (uint32_t)s);
+                    TRACE(768, kcount);
+                    kcount++;
+                    if (++s == kStages) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+                if (ok && tail_kk != 0) {
+                    // K tail: a last stage of fewer than 4 K-steps
+                    if (!mbar_wait_warp(full0 + 8u * (uint32_t)s, ph, abort_flag, args.status, 3)) {
+                        ok = false;
                     } else {
-                        // K tail: fewer than 4 K-steps
-                        for (int kk = 0; kk < nkk; kk++) {
+                        tc_fence_after();
+                        const uint32_t soff = (uint32_t)s * (kStageBytes >> 4);
+                        const uint32_t a_lo = desc_a_lo + soff;
+                        const uint32_t b_lo = a_lo + (kABytes >> 4);
+                        const uint32_t f_lo = desc_sf_lo + soff;
+                        const uint32_t sf_stage = tmem + kAccCols + (uint32_t)s * kSfColsPerStage;
+                        for (int kk = 0; kk < tail_kk; kk++) {
                             const uint32_t c = sf_stage + (uint32_t)kk * kSfColsPerKK;
                             const uint32_t f = f_lo + (uint32_t)kk * (kSfTile >> 4);
                             tmem_copy_sf_warp(c, desc_from(f, desc_sf_hi));
                             tmem_copy_sf_warp(c + 4, desc_from(f + (kSfaBytes >> 4), desc_sf_hi));
                             tmem_copy_sf_warp(c + 8, desc_from(f + ((kSfaBytes + 4 * kSfTile) >> 4), desc_sf_hi));
                         }
-                        for (int kk = 0; kk < nkk; kk++) {
+                        for (int kk = 0; kk < tail_kk; kk++) {
                             const uint32_t c = sf_stage + (uint32_t)kk * kSfColsPerKK;
                             mma_mxf4nvf4_warp(tmem, desc_from(a_lo + 2u * kk, desc_sw_hi),
                                               desc_from(b_lo + 2u * kk, desc_sw_hi), kIdesc, c, c + 4,
-                                              (kb | kk) != 0 ? 1u : 0u);
+                                              (full_kstages | kk) != 0 ? 1u : 0u);
                         }
-                    }
-                    mma_commit_warp(empty0 + 8u * (uint32_t)s);
-                    if (lane == 0) TRACE(768, kcount);
-                    kcount++;
-                    if (++s == kStages) {
-                        s = 0;
-                        ph ^= 1u;
+                        mma_commit_warp(empty0 + 8u * (uint32_t)s);
+                        kcount++;
+                        if (++s == kStages) {
+                            s = 0;
+                            ph ^= 1u;
+                        }
                     }
                 }
                 if (!ok) break;

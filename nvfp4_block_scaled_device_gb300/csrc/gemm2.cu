@@ -91,18 +91,6 @@ struct Ctrl {
 };
 static_assert(sizeof(Ctrl) <= kCtrlBytes, "control block");
 
-// The 12 scale-tile copies of a full stage, issued for both CTAs.
-__device__ __forceinline__ void issue_sf4_pair(uint32_t c, uint32_t f, uint32_t hi)
-{
-    constexpr uint32_t kB0 = kSfaBytes >> 4, kB1 = (kSfaBytes + 4 * kSfTile) >> 4, kT = kSfTile >> 4;
-#pragma unroll
-    for (int kk = 0; kk < 4; kk++) {
-        tmem_copy_sf2_warp(c + kk * kSfColsPerKK, desc_from(f + kk * kT, hi));
-        tmem_copy_sf2_warp(c + kk * kSfColsPerKK + 4, desc_from(f + kk * kT + kB0, hi));
-        tmem_copy_sf2_warp(c + kk * kSfColsPerKK + 8, desc_from(f + kk * kT + kB1, hi));
-    }
-}
-
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
     gemm2_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b0,
                  const __grid_constant__ CUtensorMap map_b1, const GemmArgs args)
@@ -126,6 +114,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
     const int64_t pair = blockIdx.x >> 1, num_pairs = gridDim.x >> 1;
     const int num_kk = (int)(args.K / 64);
     const int num_kstages = (num_kk + 3) / 4;
+    const int full_kstages = num_kk / 4;       // stages of 4 K-steps
+    const int tail_kk = num_kk % 4;            // K-steps of a last, partial stage
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; s++) {
@@ -259,65 +249,59 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
                     if (!mbar_wait_cluster_warp(smem_u32(&ctrl->acc_empty), acc_ph ^ 1u, abort_flag, args.status, 12))
                         break;
                     tc_fence_after();
-                    for (int kb = 0; kb < num_kstages; kb++) {
-                        if (!mbar_wait_warp(full0 + 8u * (uint32_t)s, ph, abort_flag, args.status, 13)) {
+                    // full stages: nothing but the waits and one fused issue block
+                    for (int kb = 0; kb < full_kstages; kb++) {
+                        if (!mbar_wait_warp(full0 + 8u * (uint32_t)s, ph, abort_flag, args.status, 13) ||
+                            !mbar_wait_cluster_warp(peer_full0 + 8u * (uint32_t)s, ph, abort_flag, args.status, 14)) {
                             ok = false;
                             break;
                         }
-                        if (lane == 0) TRACE2(1024, kcount);
-                        if (!mbar_wait_cluster_warp(peer_full0 + 8u * (uint32_t)s, ph, abort_flag, args.status, 14)) {
-                            ok = false;
-                            break;
-                        }
-                        if (lane == 0) TRACE2(1280, kcount);
+                        TRACE2(1280, kcount);
                         tc_fence_after();
                         const uint32_t soff = (uint32_t)s * (kStageBytes >> 4);
                         const uint32_t a_lo = desc_a_lo + soff;
-                        const uint32_t b_lo = a_lo + (kABytes >> 4);
-                        const uint32_t f_lo = desc_sf_lo + soff;
-                        const uint32_t sf_stage = tmem + kAccCols + (uint32_t)s * kSfColsPerStage;
-                        const int nkk = min(4, num_kk - kb * 4);
-                        const uint32_t acc0 = kb != 0 ? 1u : 0u;
-                        if (nkk == 4) {
-                            issue_sf4_pair(sf_stage, f_lo, desc_sf_hi);
-#ifdef NVFP4_TRACE
-                            if (lane == 0 && blockIdx.x < 2 && kcount < 64) g_trace2[1800 + kcount] = globaltimer();
-#endif
-                            mma2_mxf4nvf4_warp(tmem, desc_from(a_lo, desc_sw_hi), desc_from(b_lo, desc_sw_hi), kIdesc2,
-                                               sf_stage, sf_stage + 4, acc0);
-#ifdef NVFP4_TRACE
-                            if (lane == 0 && blockIdx.x < 2 && kcount < 64) g_trace2[1864 + kcount] = globaltimer();
-#endif
-                            mma2_mxf4nvf4_warp(tmem, desc_from(a_lo + 2u, desc_sw_hi), desc_from(b_lo + 2u, desc_sw_hi),
-                                               kIdesc2, sf_stage + kSfColsPerKK, sf_stage + kSfColsPerKK + 4, 1u);
-                            mma2_mxf4nvf4_warp(tmem, desc_from(a_lo + 4u, desc_sw_hi), desc_from(b_lo + 4u, desc_sw_hi),
-                                               kIdesc2, sf_stage + 2 * kSfColsPerKK, sf_stage + 2 * kSfColsPerKK + 4,
-                                               1u);
-                            mma2_mxf4nvf4_warp(tmem, desc_from(a_lo + 6u, desc_sw_hi), desc_from(b_lo + 6u, desc_sw_hi),
-                                               kIdesc2, sf_stage + 3 * kSfColsPerKK, sf_stage + 3 * kSfColsPerKK + 4,
-                                               1u);
+                        stage_issue_2sm(tmem, tmem + kAccCols + (uint32_t)s * kSfColsPerStage, desc_sf_lo + soff,
+                                        desc_sf_hi, a_lo, a_lo + (kABytes >> 4), desc_sw_hi, kIdesc2,
+                                        kb != 0 ? 1u : 0u, empty0 + 8u * (uint32_t)s, kPairMask);
+                        TRACE2(1536, kcount);
+                        kcount++;
+                        if (++s == kStages) {
+                            s = 0;
+                            ph ^= 1u;
+                        }
+                    }
+                    if (ok && tail_kk != 0) {
+                        // K tail: a last stage of fewer than 4 K-steps
+                        if (!mbar_wait_warp(full0 + 8u * (uint32_t)s, ph, abort_flag, args.status, 13) ||
+                            !mbar_wait_cluster_warp(peer_full0 + 8u * (uint32_t)s, ph, abort_flag, args.status, 14)) {
+                            ok = false;
                         } else {
-                            for (int kk = 0; kk < nkk; kk++) {
+                            tc_fence_after();
+                            const uint32_t soff = (uint32_t)s * (kStageBytes >> 4);
+                            const uint32_t a_lo = desc_a_lo + soff;
+                            const uint32_t b_lo = a_lo + (kABytes >> 4);
+                            const uint32_t f_lo = desc_sf_lo + soff;
+                            const uint32_t sf_stage = tmem + kAccCols + (uint32_t)s * kSfColsPerStage;
+                            for (int kk = 0; kk < tail_kk; kk++) {
                                 const uint32_t c = sf_stage + (uint32_t)kk * kSfColsPerKK;
                                 const uint32_t f = f_lo + (uint32_t)kk * (kSfTile >> 4);
                                 tmem_copy_sf2_warp(c, desc_from(f, desc_sf_hi));
                                 tmem_copy_sf2_warp(c + 4, desc_from(f + (kSfaBytes >> 4), desc_sf_hi));
                                 tmem_copy_sf2_warp(c + 8, desc_from(f + ((kSfaBytes + 4 * kSfTile) >> 4), desc_sf_hi));
                             }
-                            for (int kk = 0; kk < nkk; kk++) {
+                            for (int kk = 0; kk < tail_kk; kk++) {
                                 const uint32_t c = sf_stage + (uint32_t)kk * kSfColsPerKK;
                                 mma2_mxf4nvf4_warp(tmem, desc_from(a_lo + 2u * kk, desc_sw_hi),
                                                    desc_from(b_lo + 2u * kk, desc_sw_hi), kIdesc2, c, c + 4,
-                                                   (kb | kk) != 0 ? 1u : 0u);
+                                                   (full_kstages | kk) != 0 ? 1u : 0u);
                             }
-                        }
-                        // the stage is free in both CTAs once these MMAs complete
-                        mma_commit2_mc_warp(empty0 + 8u * (uint32_t)s, kPairMask);
-                        if (lane == 0) TRACE2(1536, kcount);
-                        kcount++;
-                        if (++s == kStages) {
-                            s = 0;
-                            ph ^= 1u;
+                            // the stage is free in both CTAs once these MMAs complete
+                            mma_commit2_mc_warp(empty0 + 8u * (uint32_t)s, kPairMask);
+                            kcount++;
+                            if (++s == kStages) {
+                                s = 0;
+                                ph ^= 1u;
+                            }
                         }
                     }
                     if (!ok) break;

@@ -71,48 +71,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
     return ok != 0;
 }
 
-// try_wait that may suspend the thread (no issue slots used) for up to
-// `hint_ns` while the phase is incomplete; it returns as soon as the phase
-// completes.
-__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns)
-{
-    uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n"
-        " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
-        " selp.u32 %0, 1, 0, p;\n}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity), "r"(hint_ns)
-        : "memory");
-    return ok != 0;
-}
-
-// Wait for phase `parity` of an mbarrier, giving up after about
-// kWaitLimitCycles SM clock cycles (~2 s) or as soon as another warp of the
-// CTA has given up (`abort_flag` != 0).  On giving up it raises the CTA's
-// abort flag and records kErrTimeout*100 + site in the device status word;
-// returns false.  The limit uses the SM cycle counter (cheap to read) and is
-// checked only every 64 polls, so a healthy wait costs only try_wait polls.
+// Waits give up after about kWaitLimitCycles SM clock cycles (~2 s at
+// 2 GHz): the SM cycle counter is cheap to read, and a healthy wait never
+// comes near the limit.
 constexpr uint64_t kWaitLimitCycles = 4000000000ull;
-
-template <bool kSleep = false>
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                          int* status, int site)
-{
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = clock64();
-    for (uint32_t i = 1;; i++) {
-        if (kSleep ? mbar_try_wait_sleep(bar, parity, 20000u) : mbar_try_wait(bar, parity)) return true;
-        if ((i & 63u) == 0) {
-            if (*abort_flag) return false;
-            if ((uint64_t)(clock64() - t0) > kWaitLimitCycles) {
-                *abort_flag = 1;
-                if (status) atomicCAS(status, 0, kErrTimeout * 100 + site);
-                return false;
-            }
-        }
-    }
-}
 
 // Bounded wait that ignores the abort flag (used while tearing down).
 __device__ __forceinline__ void mbar_wait_teardown(uint32_t bar, uint32_t parity)
@@ -321,66 +283,141 @@ __device__ __forceinline__ void bulk_load_warp(uint32_t dst, const void* src, ui
         : "memory");
 }
 
-// Converged fast path of a warp-wide wait: every lane polls, a vote makes
-// the outcome warp-uniform, and the loop stays inside one asm block, so a
-// warp issuing tensor-core instructions meets no divergent branch.  Gives up
-// (returns false) after kFastPolls incomplete polls.
+// Warp-wide waits.  The whole warp polls, converged: a vote makes each
+// poll's outcome warp-uniform and a round of polls runs inside one asm block.
+// A wait that leaves some lanes spinning while others idle (one lane polling
+// for the warp) slows the tensor pipe's intake of the MMA-issuing warp, even
+// from another sub-partition; a converged warp does not.  With kSleep the
+// polls carry a suspend-time hint, so a warp waiting through a whole tile
+// (the epilogue) mostly sleeps.  Between rounds the warp checks, uniformly,
+// the CTA's abort flag and the time limit (see mbar_wait).
 constexpr uint32_t kFastPolls = 256;
+constexpr uint32_t kSleepPolls = 16;
+constexpr uint32_t kSuspendHintNs = 20000;
 
+template <bool kSleep>
 __device__ __forceinline__ bool mbar_poll_warp(uint32_t bar, uint32_t parity)
 {
     uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p, q;\n .reg .u32 n;\n mov.u32 n, 0;\n"
-        "POLL_%=:\n"
-        " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-        " vote.sync.all.pred p, p, 0xffffffff;\n"
-        " @p bra.uni DONE_%=;\n"
-        " add.u32 n, n, 1;\n"
-        " setp.lt.u32 q, n, %3;\n"
-        " @q bra.uni POLL_%=;\n"
-        "DONE_%=:\n"
-        " selp.u32 %0, 1, 0, p;\n}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity), "n"(kFastPolls)
-        : "memory");
+    if (kSleep)
+        asm volatile(
+            "{\n .reg .pred p, q;\n .reg .u32 n;\n mov.u32 n, 0;\n"
+            "POLL_%=:\n"
+            " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %4;\n"
+            " vote.sync.all.pred p, p, 0xffffffff;\n"
+            " @p bra.uni DONE_%=;\n"
+            " add.u32 n, n, 1;\n"
+            " setp.lt.u32 q, n, %3;\n"
+            " @q bra.uni POLL_%=;\n"
+            "DONE_%=:\n"
+            " selp.u32 %0, 1, 0, p;\n}"
+            : "=r"(ok)
+            : "r"(bar), "r"(parity), "n"(kSleepPolls), "r"(kSuspendHintNs)
+            : "memory");
+    else
+        asm volatile(
+            "{\n .reg .pred p, q;\n .reg .u32 n;\n mov.u32 n, 0;\n"
+            "POLL_%=:\n"
+            " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+            " vote.sync.all.pred p, p, 0xffffffff;\n"
+            " @p bra.uni DONE_%=;\n"
+            " add.u32 n, n, 1;\n"
+            " setp.lt.u32 q, n, %3;\n"
+            " @q bra.uni POLL_%=;\n"
+            "DONE_%=:\n"
+            " selp.u32 %0, 1, 0, p;\n}"
+            : "=r"(ok)
+            : "r"(bar), "r"(parity), "n"(kFastPolls)
+            : "memory");
     return ok != 0;
 }
 
-// As mbar_poll_warp, with cluster-scope acquire.
+// As mbar_poll_warp, with cluster-scope acquire (phases completed by the
+// other CTA of the pair).
+template <bool kSleep>
 __device__ __forceinline__ bool mbar_poll_cluster_warp(uint32_t bar, uint32_t parity)
 {
     uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p, q;\n .reg .u32 n;\n mov.u32 n, 0;\n"
-        "POLL_%=:\n"
-        " mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
-        " vote.sync.all.pred p, p, 0xffffffff;\n"
-        " @p bra.uni DONE_%=;\n"
-        " add.u32 n, n, 1;\n"
-        " setp.lt.u32 q, n, %3;\n"
-        " @q bra.uni POLL_%=;\n"
-        "DONE_%=:\n"
-        " selp.u32 %0, 1, 0, p;\n}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity), "n"(kFastPolls)
-        : "memory");
+    if (kSleep)
+        asm volatile(
+            "{\n .reg .pred p, q;\n .reg .u32 n;\n mov.u32 n, 0;\n"
+            "POLL_%=:\n"
+            " mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %4;\n"
+            " vote.sync.all.pred p, p, 0xffffffff;\n"
+            " @p bra.uni DONE_%=;\n"
+            " add.u32 n, n, 1;\n"
+            " setp.lt.u32 q, n, %3;\n"
+            " @q bra.uni POLL_%=;\n"
+            "DONE_%=:\n"
+            " selp.u32 %0, 1, 0, p;\n}"
+            : "=r"(ok)
+            : "r"(bar), "r"(parity), "n"(kSleepPolls), "r"(kSuspendHintNs)
+            : "memory");
+    else
+        asm volatile(
+            "{\n .reg .pred p, q;\n .reg .u32 n;\n mov.u32 n, 0;\n"
+            "POLL_%=:\n"
+            " mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+            " vote.sync.all.pred p, p, 0xffffffff;\n"
+            " @p bra.uni DONE_%=;\n"
+            " add.u32 n, n, 1;\n"
+            " setp.lt.u32 q, n, %3;\n"
+            " @q bra.uni POLL_%=;\n"
+            "DONE_%=:\n"
+            " selp.u32 %0, 1, 0, p;\n}"
+            : "=r"(ok)
+            : "r"(bar), "r"(parity), "n"(kFastPolls)
+            : "memory");
     return ok != 0;
 }
 
-// Warp-wide bounded wait: the converged fast path first; if the phase is
-// still incomplete, lane 0 keeps polling (bounded, see mbar_wait), the
-// result is broadcast and the warp leaves converged.
+// Bounded warp-wide wait (converged throughout).  On giving up it raises the
+// CTA's abort flag and records kErrTimeout*100 + site in the device status
+// word (a timeout), or leaves them as they are (another warp gave up first);
+// returns false.
 template <bool kSleep = false>
 __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* status,
                                                int site)
 {
-    if (!kSleep && mbar_poll_warp(bar, parity)) return true;
-    int ok = 1;
-    if ((threadIdx.x & 31) == 0) ok = mbar_wait<kSleep>(bar, parity, abort_flag, status, site) ? 1 : 0;
-    ok = __shfl_sync(0xffffffffu, ok, 0);
-    __syncwarp();
-    return ok != 0;
+    if (mbar_poll_warp<kSleep>(bar, parity)) return true;
+    const uint64_t t0 = clock64();
+    for (;;) {
+        if (mbar_poll_warp<kSleep>(bar, parity)) return true;
+        // every lane reads the flag and the clock; lane 0's verdict is the warp's
+        int stop = *abort_flag ? 1 : ((uint64_t)(clock64() - t0) > kWaitLimitCycles ? 2 : 0);
+        stop = __shfl_sync(0xffffffffu, stop, 0);
+        if (stop != 0) {
+            if (stop == 2 && (threadIdx.x & 31) == 0) {
+                *abort_flag = 1;
+                if (status) atomicCAS(status, 0, kErrTimeout * 100 + site);
+            }
+            __syncwarp();
+            return false;
+        }
+    }
+}
+
+// As mbar_wait_warp, with cluster-scope acquire.
+template <bool kSleep = false>
+__device__ __forceinline__ bool mbar_wait_cluster_warp(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* status,
+                                                       int site)
+{
+    if (mbar_poll_cluster_warp<kSleep>(bar, parity)) return true;
+    const uint64_t t0 = clock64();
+    for (;;) {
+        if (mbar_poll_cluster_warp<kSleep>(bar, parity)) return true;
+        // every lane reads the flag and the clock; lane 0's verdict is the warp's
+        int stop = *abort_flag ? 1 : ((uint64_t)(clock64() - t0) > kWaitLimitCycles ? 2 : 0);
+        stop = __shfl_sync(0xffffffffu, stop, 0);
+        if (stop != 0) {
+            if (stop == 2 && (threadIdx.x & 31) == 0) {
+                *abort_flag = 1;
+                if (status) atomicCAS(status, 0, kErrTimeout * 100 + site);
+            }
+            __syncwarp();
+            return false;
+        }
+    }
 }
 
 // Arrive on an mbarrier once all tcgen05 operations issued so far by this
@@ -438,63 +475,6 @@ __device__ __forceinline__ void cluster_sync_all()
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr)
 {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
-}
-
-// try_wait with cluster-scope acquire; with kSleep the thread may suspend
-// (no issue slots used) until the phase completes or about 20 us pass.
-template <bool kSleep>
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity)
-{
-    uint32_t ok;
-    if (kSleep)
-        asm volatile(
-            "{\n .reg .pred p;\n"
-            " mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n"
-            " selp.u32 %0, 1, 0, p;\n}"
-            : "=r"(ok)
-            : "r"(bar), "r"(parity), "r"(20000u)
-            : "memory");
-    else
-        asm volatile(
-            "{\n .reg .pred p;\n"
-            " mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
-            " selp.u32 %0, 1, 0, p;\n}"
-            : "=r"(ok)
-            : "r"(bar), "r"(parity)
-            : "memory");
-    return ok != 0;
-}
-
-// Warp-wide bounded wait with cluster-scope acquire (for phases completed
-// by the other CTA of the pair): the converged fast path first, then lane 0
-// polls, the result is broadcast and the warp leaves converged.
-template <bool kSleep = false>
-__device__ __forceinline__ bool mbar_wait_cluster_warp(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                                       int* status, int site)
-{
-    if (!kSleep && mbar_poll_cluster_warp(bar, parity)) return true;
-    int ok = 1;
-    if ((threadIdx.x & 31) == 0) {
-        ok = 0;
-        const uint64_t t0 = clock64();
-        for (uint32_t i = 0;; i++) {
-            if (mbar_try_wait_cluster<kSleep>(bar, parity)) {
-                ok = 1;
-                break;
-            }
-            if ((i & 63u) == 63u) {
-                if (*abort_flag) break;
-                if ((uint64_t)(clock64() - t0) > kWaitLimitCycles) {
-                    *abort_flag = 1;
-                    if (status) atomicCAS(status, 0, kErrTimeout * 100 + site);
-                    break;
-                }
-            }
-        }
-    }
-    ok = __shfl_sync(0xffffffffu, ok, 0);
-    __syncwarp();
-    return ok != 0;
 }
 
 // 2-SM (cta_group::2) tensor-core operations: issued by the pair's even CTA

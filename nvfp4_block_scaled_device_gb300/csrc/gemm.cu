@@ -63,6 +63,7 @@ constexpr int kNumThreads = 512;
 constexpr uint32_t kRegsSmall = 56;
 constexpr uint32_t kRegsEpi = 200;
 static_assert(2 * kRegsSmall + 2 * kRegsEpi == 512, "register split per sub-partition");
+static_assert(kProducers == kEpiWarp0 - 1, "producers: warpgroups 0-1 less the MMA warp");
 
 // Instruction descriptor, kind::mxf4nvf4: A and B E2M1 (format 1), UE4M3
 // scales (bit 23 = 0), K-major A and B, N = 256 (bits 17-22 = N/8),
@@ -117,7 +118,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; s++) {
-            mbar_init(smem_u32(&ctrl->full[s]), kProducers);
+            mbar_init(smem_u32(&ctrl->full[s]), 1);      // producer 0's arrival + all copies' bytes
             mbar_init(smem_u32(&ctrl->empty[s]), 1);
         }
         mbar_init(smem_u32(&ctrl->acc_full), 1);
@@ -149,10 +150,15 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             // issued by one thread are served one after the other, about 25
             // bytes per clock): producer p < 6 fetches the 64-row code box p of
             // the stage (A rows 0-63, 64-127, B rows 0-63, ..., 192-255), producer
-            // 6 the A and B scale tiles.  Each arrives once per stage on the full
-            // barrier with its own byte count.  A box whose first row is past the
-            // operand's rows is not fetched: its stale shared memory only feeds
-            // accumulator rows >= M or columns >= N, never stored.
+            // 6 the A and B scale tiles.  Producer 0 alone arrives on the stage's
+            // full barrier, with the byte count of all seven producers' copies;
+            // the others' copies only complete bytes on it, so the stage is full
+            // when every byte has landed, whatever order the producers run in
+            // (a slot is refilled only after the MMAs that read it completed,
+            // so no copy of a later fill can land in the current phase).  A box
+            // whose first row is past the operand's rows is not fetched: its
+            // stale shared memory only feeds accumulator rows >= M or columns
+            // >= N, never stored.
             const int p = warp < kMmaWarp ? warp : warp - 1;
             const uint32_t full0 = smem_u32(&ctrl->full[0]);
             const uint32_t empty0 = smem_u32(&ctrl->empty[0]);
@@ -184,6 +190,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 const CUtensorMap* my_map = p < 2 ? &map_a : p < 4 ? &map_b0 : (swiglu ? &map_b1 : &map_b0);
                 const int32_t my_y = (p < 2 ? ya : p < 4 ? yb0 : yb1) + (p & 1) * kCodeBoxRows;
                 const bool my_box = p < 6 && my_y < (p < 2 ? args.M : args.N);
+                // code boxes of the stage that are fetched (A rows +64, B rows +64, +128, +192)
+                const uint32_t code_bytes =
+                    kBox * (1u + (ya + kCodeBoxRows < args.M ? 1u : 0u) + 1u + (yb0 + kCodeBoxRows < args.N ? 1u : 0u) +
+                            (yb1 < args.N ? 1u : 0u) + (yb1 + kCodeBoxRows < args.N ? 1u : 0u));
                 const uint8_t* pa = args.sfa + mt * args.sfa_tile_stride;
                 for (int kb = 0; kb < num_kstages; kb++) {
                     if (!mbar_wait_warp(empty0 + 8u * (uint32_t)s, ph ^ 1u, abort_flag, args.status, 1)) {
@@ -192,23 +202,18 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     }
                     if (p == 0 && lane == 0) TRACE(0, kcount);
                     const uint32_t sf_bytes = (uint32_t)min(4, num_kk - kb * 4) * kSfTile;
-                    const uint32_t tx = my_box ? kBox : p == 6 ? sf_bytes * (has_b1 ? 3u : 2u) : 0u;
                     const uint32_t full = full0 + 8u * (uint32_t)s;
                     const uint32_t st = base + (uint32_t)s * kStageBytes;
                     const uint32_t sf_st = st + kABytes + kBBytes;
                     const int32_t xk = kb * 128;
                     if (lane == 0) {
-                        if (tx == 0) {
-                            mbar_arrive(full);
-                        } else {
-                            mbar_arrive_expect_tx(full, tx);
-                            if (my_box) {
-                                tma_load_2d(st + my_off, my_map, full, xk, my_y, pol);
-                            } else {
-                                bulk_load(sf_st, pa, sf_bytes, full);
-                                bulk_load(sf_st + kSfaBytes, pb0, sf_bytes, full);
-                                if (has_b1) bulk_load(sf_st + kSfaBytes + 4 * kSfTile, pb1, sf_bytes, full);
-                            }
+                        if (p == 0) mbar_arrive_expect_tx(full, code_bytes + sf_bytes * (has_b1 ? 3u : 2u));
+                        if (my_box) {
+                            tma_load_2d(st + my_off, my_map, full, xk, my_y, pol);
+                        } else if (p == 6) {
+                            bulk_load(sf_st, pa, sf_bytes, full);
+                            bulk_load(sf_st + kSfaBytes, pb0, sf_bytes, full);
+                            if (has_b1) bulk_load(sf_st + kSfaBytes + 4 * kSfTile, pb1, sf_bytes, full);
                         }
                     }
                     __syncwarp();
@@ -331,12 +336,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         int ecount = 0;
         for (int64_t tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
             const int64_t mt = tile % num_m, nt = tile / num_m;
-            // one lane waits; the warp then proceeds converged (tcgen05.ld is warp-wide)
-            int ok = 1;
-            if (lane == 0) ok = mbar_wait<true>(smem_u32(&ctrl->acc_full), acc_ph, abort_flag, args.status, 4) ? 1 : 0;
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            __syncwarp();
-            if (!ok) break;
+            if (!mbar_wait_warp<true>(smem_u32(&ctrl->acc_full), acc_ph, abort_flag, args.status, 4)) break;
             if (warp == kEpiWarp0 && lane == 0) TRACE(1088, ecount);
             tc_fence_after();
             float v[128];

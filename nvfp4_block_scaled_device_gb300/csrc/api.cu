@@ -78,6 +78,21 @@ int make_codes_map(CUtensorMap* m, const void* base, int64_t rows, int64_t row_b
     return r == CUDA_SUCCESS ? NVFP4_OK : NVFP4_ERR_CUDA;
 }
 
+// Scale factors viewed as a 1-D array of 8-byte elements, boxes of 256
+// elements: one box is the 2048 contiguous bytes of four 512-byte scale
+// tiles (one K stage of a 128-row block).
+int make_sf_map(CUtensorMap* m, const void* base, size_t bytes)
+{
+    cuuint64_t dims[1] = {(cuuint64_t)(bytes / 8)};
+    cuuint64_t strides[1] = {0};
+    cuuint32_t box[1] = {256};
+    cuuint32_t estr[1] = {1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT64, 1, const_cast<void*>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? NVFP4_OK : NVFP4_ERR_CUDA;
+}
+
 inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 inline int64_t pad_to(int64_t v, int64_t m) { return (v + m - 1) / m * m; }
 inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
@@ -113,14 +128,23 @@ int64_t sf_tile_stride(int64_t cols) { return pad_to(cols / 16, 4) / 4 * 512; }
     } while (0)
 
 // The SM-pair kernel (256-row tiles) takes M >= kPairMinRows; below that,
-// one 128-row tile per CTA.  The pair kernel currently measures slower than
-// the 1-SM kernel at every block shape, so the threshold is set above any M.
+// one 128-row tile per CTA.  Over the prefill block's four GEMM shapes the
+// pair kernel is slower in sum (faster on the deep-K down projection, slower
+// on the others), so the threshold is set above any M.
 constexpr int64_t kPairMinRows = INT64_MAX;
 
 cudaError_t run_gemm(const CUtensorMap& ma, const CUtensorMap& mb0, const CUtensorMap& mb1, const GemmArgs& a,
                      const DeviceInfo* d, cudaStream_t stream)
 {
-    if (a.M >= kPairMinRows) return launch_gemm2(ma, mb0, mb1, a, d->num_sms, stream);
+    if (a.M >= kPairMinRows) {
+        // the pair kernel fetches the scale tiles through tensor maps too
+        CUtensorMap msa, msb0, msb1;
+        if (make_sf_map(&msa, a.sfa, nvfp4_sf_bytes(a.M, a.K)) != NVFP4_OK ||
+            make_sf_map(&msb0, a.sfb0, nvfp4_sf_bytes(a.N, a.K)) != NVFP4_OK ||
+            make_sf_map(&msb1, a.sfb1 ? a.sfb1 : a.sfb0, nvfp4_sf_bytes(a.N, a.K)) != NVFP4_OK)
+            return cudaErrorInvalidValue;
+        return launch_gemm2(ma, mb0, mb1, msa, msb0, msb1, a, d->num_sms, stream);
+    }
     return launch_gemm(ma, mb0, mb1, a, d->num_sms, stream);
 }
 

@@ -110,6 +110,31 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
         : "memory");
 }
 
+// tma_load_2d for an SM pair: the copy lands in this CTA's shared memory and
+// completes its bytes on `bar_cluster`, an mbarrier of either CTA of the pair
+// (a shared::cluster address), so both CTAs' copies of a stage can report
+// to one barrier of the pair's leader.
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar_cluster,
+                                                 int32_t x, int32_t y, uint64_t cache_hint)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(x), "r"(y), "l"(cache_hint)
+        : "memory");
+}
+
+// 1-D form of tma_load_2d_pair (element coordinate x).
+__device__ __forceinline__ void tma_load_1d_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar_cluster,
+                                                 int32_t x, uint64_t cache_hint)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.1d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%3}], [%2], %4;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(x), "l"(cache_hint)
+        : "memory");
+}
+
 // Warm L2 with a tensor tile (no shared-memory destination, no completion).
 __device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int32_t x, int32_t y)
 {

@@ -14,12 +14,13 @@
 // Each CTA of the pair loads, into its own shared memory: its 128 rows of A
 // and their scales, its 128-row half of B (rows 0-127 in the even CTA, rows
 // 128-255 in the odd one; for SwiGLU the W_gate and the W_up rows), and the
-// scales of all 256 B rows.  The even CTA ("leader") issues the scale copies
-// and MMAs for both CTAs once both halves of a stage have landed: the odd
-// CTA's otherwise idle MMA warp relays "stage landed" to the leader by a
-// remote mbarrier arrive.  The leader's commits are multicast to both CTAs
-// (stage free, accumulator ready); both CTAs' epilogue warps arrive on the
-// leader's accumulator-free barrier.  Each CTA's epilogue reads its own
+// scales of all 256 B rows.  Every copy of both CTAs, scale tiles included
+// (through 1-D tensor maps), completes its bytes on the full
+// barrier of the pair's even CTA ("leader"), whose producer 0 alone arrives
+// on it with the byte count of both CTAs; the leader then issues the scale
+// copies and MMAs for both CTAs.  The leader's commits are multicast to both
+// CTAs (stage free, accumulator ready); both CTAs' epilogue warps arrive on
+// the leader's accumulator-free barrier.  Each CTA's epilogue reads its own
 // tensor memory (its 128 rows of the 256-row tile).
 #include "common.cuh"
 #include "gemm_epilogue.cuh"
@@ -47,8 +48,8 @@ constexpr uint32_t kSfColsPerStage = 4 * kSfColsPerKK;
 static_assert(kAccCols + kStages * kSfColsPerStage <= kTmemCols, "tensor memory budget");
 
 // Warp roles (16 warps, 4 warpgroups): warps 0-3 and 5-7 are copy
-// producers (each a separate copy stream), warp 4 the MMA warp (leader) or
-// the stage relay (odd CTA), warps 8-15 the epilogue.  Launched at 128
+// producers (each a separate copy stream), warp 4 the MMA warp (leader; in
+// the odd CTA it only allocates tensor memory), warps 8-15 the epilogue.  Launched at 128
 // registers per thread; warpgroups 0-1 drop to 56 and 2-3 rise to 200.
 constexpr int kProducers = 7;
 constexpr int kMmaWarp = 4;
@@ -58,6 +59,7 @@ constexpr int kNumThreads = 512;
 constexpr uint32_t kRegsSmall = 56;
 constexpr uint32_t kRegsEpi = 200;
 static_assert(2 * kRegsSmall + 2 * kRegsEpi == 512, "register split per sub-partition");
+static_assert(kProducers == kEpiWarp0 - 1, "producers: warpgroups 0-1 less the MMA warp");
 constexpr uint16_t kPairMask = 0x3;            // both CTAs of the cluster
 
 // Instruction descriptor, kind::mxf4nvf4: E2M1 A and B (format 1), UE4M3
@@ -67,9 +69,8 @@ constexpr uint32_t kIdesc2 = (1u << 7) | (1u << 10) | ((256u >> 3) << 17) | ((25
 #ifdef NVFP4_TRACE
 // Debug timeline of the first CTA pair (built only with -DNVFP4_TRACE),
 // %globaltimer ns: [0,256) leader stage-free seen, [256,512) leader issued,
-// [512,768) odd stage-free seen, [768,1024) odd issued, [1024,1280) leader
-// own-full seen, [1280,1536) leader peer-full seen, [1536,1792) leader MMAs
-// issued, [1792,2048) odd relay sent.
+// [512,768) odd stage-free seen, [768,1024) odd issued, [1280,1536) leader
+// stage full seen, [1536,1792) leader MMAs issued.
 __device__ unsigned long long g_trace2[2048];
 #define TRACE2(slot, i)                                                 \
     do {                                                                \
@@ -80,8 +81,7 @@ __device__ unsigned long long g_trace2[2048];
 #endif
 
 struct Ctrl {
-    uint64_t full[kStages];       // this CTA's loads of the stage landed
-    uint64_t peer_full[kStages];  // (leader) the odd CTA's loads of the stage landed
+    uint64_t full[kStages];       // (leader) both CTAs' copies of the stage landed
     uint64_t empty[kStages];      // the pair's MMAs finished reading the stage
     uint64_t acc_full;            // the tile's accumulator is complete
     uint64_t acc_empty;           // (leader) both CTAs' epilogues drained the accumulator
@@ -93,7 +93,9 @@ static_assert(sizeof(Ctrl) <= kCtrlBytes, "control block");
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
     gemm2_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b0,
-                 const __grid_constant__ CUtensorMap map_b1, const GemmArgs args)
+                 const __grid_constant__ CUtensorMap map_b1, const __grid_constant__ CUtensorMap map_sfa,
+                 const __grid_constant__ CUtensorMap map_sfb0, const __grid_constant__ CUtensorMap map_sfb1,
+                 const GemmArgs args)
 {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
@@ -119,8 +121,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; s++) {
-            mbar_init(smem_u32(&ctrl->full[s]), kProducers);
-            mbar_init(smem_u32(&ctrl->peer_full[s]), 1);
+            mbar_init(smem_u32(&ctrl->full[s]), 1);     // leader's producer 0 + both CTAs' bytes
             mbar_init(smem_u32(&ctrl->empty[s]), 1);
         }
         mbar_init(smem_u32(&ctrl->acc_full), 1);
@@ -132,7 +133,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
     if (warp == 0 && lane == 0) {
         prefetch_tmap(&map_a);
         prefetch_tmap(&map_b0);
-        if (swiglu) prefetch_tmap(&map_b1);
+        prefetch_tmap(&map_sfa);
+        prefetch_tmap(&map_sfb0);
+        if (swiglu) {
+            prefetch_tmap(&map_b1);
+            prefetch_tmap(&map_sfb1);
+        }
     }
     if (warp == kMmaWarp) {
         tmem_alloc2(smem_u32(&ctrl->tmem_base), kTmemCols);
@@ -151,89 +157,100 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
             // ------------------------------------------------------ producers
             // Seven warps, one lane each, share every stage's copies (copies
             // issued by one thread are served one after the other): producers
-            // 0-3 fetch the 64-row code boxes (this CTA's A rows 0-63, 64-127, its
-            // B half's rows 0-63, 64-127), producers 4-6 the scale tiles (A, B
-            // rows 0-127, B rows 128-255).  Each arrives once per stage on its
-            // CTA's full barrier with its own byte count.  Boxes past the
-            // operand's rows are not fetched: their stale shared memory only
-            // feeds accumulator rows >= M or columns >= N.
+            // 0-3 fetch the 64-row code boxes (this CTA's A rows 0-63, 64-127,
+            // its B half's rows 0-63, 64-127), producers 4-6 the 2 KB scale
+            // runs (A, B rows 0-127, B rows 128-255) of the stage.  All copies
+            // complete on the leader's full barrier; the leader's producer 0
+            // arrives on it once per stage with both CTAs' byte count (a slot
+            // is refilled only after the MMAs that read it completed, so no
+            // copy of a later fill can land in the current phase).  Boxes past
+            // the operand's rows are not fetched: their stale shared memory
+            // only feeds accumulator rows >= M or columns >= N.  A scale box
+            // of a partial last stage also carries the scales of the next K
+            // stages or of the next rows (or zero fill past the end), which no
+            // MMA reads.
             const int p = warp < kMmaWarp ? warp : warp - 1;
-            const uint32_t full0 = smem_u32(&ctrl->full[0]);
+            const uint32_t full_leader0 = map_to_cta(smem_u32(&ctrl->full[0]), 0);
             const uint32_t empty0 = smem_u32(&ctrl->empty[0]);
             constexpr uint32_t kBox = kCodeBoxRows * 128u;
+            constexpr uint32_t kSfBox = 4u * kSfTile;                       // 2048 bytes
             const uint64_t pol = p < 2 ? l2_policy_evict_last() : l2_policy_evict_first();
-            const uint32_t my_off = (uint32_t)p * kBox;     // A then the B half, contiguous
+            const uint32_t my_off = p < 4 ? (uint32_t)p * kBox                // A then the B half, contiguous
+                                          : (uint32_t)(kABytes + kBBytes) + (uint32_t)(p - 4) * kSfBox;
+            const CUtensorMap* sf_map = p == 4 ? &map_sfa : (p == 6 && swiglu) ? &map_sfb1 : &map_sfb0;
             int s = 0;
-            uint32_t ph = 0, issued = 0, issued_ph = 0;
+            uint32_t ph = 0;
             bool ok = true;
             int kcount = 0;
             for (int64_t tile = pair; tile < num_tiles && ok; tile += num_pairs) {
                 const int64_t mt = tile % num_m, nt = tile / num_m;
                 const int64_t row0 = mt * 256 + rank * 128;          // this CTA's first A row
-                const bool has_a = row0 < args.M;                    // else its rows (and scale tile) do not exist
                 int32_t yb;
                 const CUtensorMap* mb;
-                const uint8_t *pb0, *pb1;
-                bool has_b1;
+                int64_t sfb_block0, sfb_block1;                      // 128-row scale blocks of B
                 if (swiglu) {
                     yb = (int32_t)(nt * 128);
                     mb = rank ? &map_b1 : &map_b0;
-                    pb0 = args.sfb0 + nt * args.sfb_tile_stride;
-                    pb1 = args.sfb1 + nt * args.sfb_tile_stride;
-                    has_b1 = true;
+                    sfb_block0 = sfb_block1 = nt;
                 } else {
                     yb = (int32_t)(nt * 256 + rank * 128);
                     mb = &map_b0;
-                    pb0 = args.sfb0 + (2 * nt) * args.sfb_tile_stride;
-                    pb1 = args.sfb0 + (2 * nt + 1) * args.sfb_tile_stride;
-                    has_b1 = nt * 256 + 128 < args.N;               // the second B scale tile exists
+                    sfb_block0 = 2 * nt;
+                    sfb_block1 = 2 * nt + 1;
                 }
-                const CUtensorMap* my_map = p < 2 ? &map_a : mb;
-                const int32_t my_y = (p < 2 ? (int32_t)row0 : yb) + (p & 1) * kCodeBoxRows;
-                const bool my_box = p < 4 && my_y < (p < 2 ? args.M : args.N);
-                const bool my_sf = p == 4 ? has_a : p == 5 ? true : p == 6 ? has_b1 : false;
-                const uint8_t* my_sf_src = p == 4 ? args.sfa + (row0 / 128) * args.sfa_tile_stride : p == 5 ? pb0 : pb1;
-                const uint32_t my_sf_off = kABytes + kBBytes + (p == 4 ? 0u : p == 5 ? (uint32_t)kSfaBytes
-                                                                                      : (uint32_t)(kSfaBytes + 4 * kSfTile));
+                const bool has_b1 = swiglu || nt * 256 + 128 < args.N;   // the second B scale block exists
+                // this producer's copy: code box (first row), or scale box
+                // (first 8-byte element of its 2 KB run at K stage 0)
+                const CUtensorMap* my_map = p < 2 ? &map_a : p < 4 ? mb : sf_map;
+                const int32_t my_y = p < 4 ? (p < 2 ? (int32_t)row0 : yb) + (p & 1) * kCodeBoxRows
+                                           : (int32_t)(((p == 4 ? (row0 / 128) * args.sfa_tile_stride
+                                                                : (p == 5 ? sfb_block0 : sfb_block1) * args.sfb_tile_stride)) /
+                                                       8);
+                const bool my_copy = p < 4 ? my_y < (p < 2 ? args.M : args.N)
+                                           : p == 4 ? row0 < args.M : p == 5 ? true : has_b1;
+                // bytes of the stage's copies in both CTAs (the leader's producer 0 expects them)
+                uint32_t tx = 0;
+                if (leader && p == 0) {
+                    for (int r = 0; r < 2; r++) {
+                        const int64_t r0 = mt * 256 + r * 128;
+                        const int64_t yr = swiglu ? nt * 128 : nt * 256 + r * 128;
+                        tx += kBox * ((r0 < args.M) + (r0 + kCodeBoxRows < args.M) + (yr < args.N) +
+                                      (yr + kCodeBoxRows < args.N));
+                        tx += kSfBox * ((r0 < args.M) + 1 + (has_b1 ? 1 : 0));
+                    }
+                }
                 for (int kb = 0; kb < num_kstages; kb++) {
                     if (!mbar_wait_cluster_warp(empty0 + 8u * (uint32_t)s, ph ^ 1u, abort_flag, args.status, 11)) {
                         ok = false;
                         break;
                     }
                     if (p == 0 && lane == 0) TRACE2(rank * 512, kcount);
-                    const uint32_t sf_bytes = (uint32_t)min(4, num_kk - kb * 4) * kSfTile;
-                    const uint32_t tx = my_box ? kBox : my_sf ? sf_bytes : 0u;
-                    const uint32_t full = full0 + 8u * (uint32_t)s;
+                    const uint32_t full = full_leader0 + 8u * (uint32_t)s;
                     const uint32_t st = base + (uint32_t)s * kStageBytes;
-                    const int32_t xk = kb * 128;
                     if (lane == 0) {
-                        if (tx == 0) {
-                            mbar_arrive(full);
-                        } else {
-                            mbar_arrive_expect_tx(full, tx);
-                            if (my_box) tma_load_2d(st + my_off, my_map, full, xk, my_y, pol);
-                            else bulk_load(st + my_sf_off, my_sf_src + (size_t)kb * (4 * kSfTile), sf_bytes, full);
+                        if (leader && p == 0) mbar_arrive_expect_tx(smem_u32(&ctrl->full[0]) + 8u * (uint32_t)s, tx);
+                        if (my_copy) {
+                            if (p < 4)
+                                tma_load_2d_pair(st + my_off, my_map, full, kb * 128, my_y, pol);
+                            else
+                                tma_load_1d_pair(st + my_off, my_map, full, my_y + kb * (int32_t)(kSfBox / 8), pol);
                         }
                     }
                     __syncwarp();
                     if (p == 0 && lane == 0) TRACE2(rank * 512 + 256, kcount);
                     kcount++;
-                    issued |= 1u << s;
-                    issued_ph = (issued_ph & ~(1u << s)) | (ph << s);
                     if (++s == kStages) {
                         s = 0;
                         ph ^= 1u;
                     }
                 }
             }
-            if (!ok && lane == 0) {
-                for (int i = 0; i < kStages; i++)
-                    if (issued & (1u << i)) mbar_wait_teardown(full0 + 8u * (uint32_t)i, (issued_ph >> i) & 1u);
-            }
+            // on an early stop, the leader's teardown waits for the copies in
+            // flight (its full barriers count both CTAs' bytes); the final
+            // cluster barrier keeps this CTA alive until then
             __syncwarp();
         } else {
             const uint32_t full0 = smem_u32(&ctrl->full[0]);
-            const uint32_t peer_full0 = smem_u32(&ctrl->peer_full[0]);
             const uint32_t empty0 = smem_u32(&ctrl->empty[0]);
             if (leader) {
                 // ----------------------------------------------- MMA (pair)
@@ -249,10 +266,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
                     if (!mbar_wait_cluster_warp(smem_u32(&ctrl->acc_empty), acc_ph ^ 1u, abort_flag, args.status, 12))
                         break;
                     tc_fence_after();
-                    // full stages: nothing but the waits and one fused issue block
+                    // full stages: nothing but the wait and one fused issue block
                     for (int kb = 0; kb < full_kstages; kb++) {
-                        if (!mbar_wait_warp(full0 + 8u * (uint32_t)s, ph, abort_flag, args.status, 13) ||
-                            !mbar_wait_cluster_warp(peer_full0 + 8u * (uint32_t)s, ph, abort_flag, args.status, 14)) {
+                        if (!mbar_wait_cluster_warp(full0 + 8u * (uint32_t)s, ph, abort_flag, args.status, 13)) {
                             ok = false;
                             break;
                         }
@@ -272,8 +288,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
                     }
                     if (ok && tail_kk != 0) {
                         // K tail: a last stage of fewer than 4 K-steps
-                        if (!mbar_wait_warp(full0 + 8u * (uint32_t)s, ph, abort_flag, args.status, 13) ||
-                            !mbar_wait_cluster_warp(peer_full0 + 8u * (uint32_t)s, ph, abort_flag, args.status, 14)) {
+                        if (!mbar_wait_cluster_warp(full0 + 8u * (uint32_t)s, ph, abort_flag, args.status, 13)) {
                             ok = false;
                         } else {
                             tc_fence_after();
@@ -311,30 +326,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
                 // every MMA issued has completed before teardown
                 mma_commit2_mc_warp(smem_u32(&ctrl->teardown), 0x1);
                 if (lane == 0) mbar_wait_teardown(smem_u32(&ctrl->teardown), 0);
-                __syncwarp();
-            } else {
-                // ------------------------------ relay (odd CTA): stage landed
-                const uint32_t leader_peer_full0 = map_to_cta(peer_full0, 0);
-                int s = 0;
-                uint32_t ph = 0;
-                bool ok = true;
-                int kcount = 0;
-                for (int64_t tile = pair; tile < num_tiles && ok; tile += num_pairs) {
-                    for (int kb = 0; kb < num_kstages; kb++) {
-                        if (!mbar_wait_warp(full0 + 8u * (uint32_t)s, ph, abort_flag, args.status, 15)) {
-                            ok = false;
-                            break;
-                        }
-                        if (lane == 0) mbar_arrive_remote(leader_peer_full0 + 8u * (uint32_t)s);
-                        if (lane == 0 && kcount < 8) TRACE2(1792, kcount);
-                        kcount++;
-                        __syncwarp();
-                        if (++s == kStages) {
-                            s = 0;
-                            ph ^= 1u;
-                        }
+                if (!ok && lane == 0) {
+                    // stopped early: let the copies of the stages not consumed
+                    // land in both CTAs before their shared memory goes away
+                    // (bounded); the next fill of each slot (phase ph of slot s
+                    // onwards) may be in flight
+                    for (int i = 0; i < kStages; i++) {
+                        const int si = (s + i) % kStages;
+                        const uint32_t pi = si >= s ? ph : ph ^ 1u;
+                        mbar_wait_teardown(full0 + 8u * (uint32_t)si, pi);
                     }
                 }
+                __syncwarp();
             }
         }
     } else {
@@ -394,6 +397,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
 }  // namespace
 
 cudaError_t launch_gemm2(const CUtensorMap& map_a, const CUtensorMap& map_b0, const CUtensorMap& map_b1,
+                         const CUtensorMap& map_sfa, const CUtensorMap& map_sfb0, const CUtensorMap& map_sfb1,
                          const GemmArgs& args, int num_sms, cudaStream_t stream)
 {
     static int attr_set_for_device[64] = {0};
@@ -410,7 +414,8 @@ cudaError_t launch_gemm2(const CUtensorMap& map_a, const CUtensorMap& map_b0, co
     const int64_t num_n = swiglu ? args.N / 128 : (args.N + 255) / 256;
     const int64_t tiles = num_m * num_n;
     const int64_t pairs = tiles < num_sms / 2 ? tiles : num_sms / 2;
-    gemm2_kernel<<<(unsigned)(2 * pairs), kNumThreads, kSmemBytes, stream>>>(map_a, map_b0, map_b1, args);
+    gemm2_kernel<<<(unsigned)(2 * pairs), kNumThreads, kSmemBytes, stream>>>(map_a, map_b0, map_b1, map_sfa,
+                                                                              map_sfb0, map_sfb1, args);
     return cudaGetLastError();
 }
 

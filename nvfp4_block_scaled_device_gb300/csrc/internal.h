@@ -75,9 +75,11 @@ struct GemmArgs {
 cudaError_t launch_gemm(const CUtensorMap& map_a, const CUtensorMap& map_b0, const CUtensorMap& map_b1,
                         const GemmArgs& args, int num_sms, cudaStream_t stream);
 
-// 2-SM version (clusters of 2 CTAs, 256-row tiles): same arguments and
-// results; used for M > 128.
+// SM-pair version (clusters of 2 CTAs, 256-row tiles): same arguments and
+// results, plus 1-D tensor maps of the scale factors of A, B0 and B1 (8-byte
+// elements, boxes of 256 elements = 2048 bytes).
 cudaError_t launch_gemm2(const CUtensorMap& map_a, const CUtensorMap& map_b0, const CUtensorMap& map_b1,
+                         const CUtensorMap& map_sfa, const CUtensorMap& map_sfb0, const CUtensorMap& map_sfb1,
                          const GemmArgs& args, int num_sms, cudaStream_t stream);
 
 size_t gemm_smem_bytes();

@@ -311,9 +311,9 @@ def run_ours(args):
                     nv.nvfp4_gemm_swiglu(blk.hm, W["gate"], W["up"], nv.NVFP4_INTER_STATIC, blk.g_inter, blk.s,
                                          blk.ws_swiglu, None, stream)
                 elif args.only == "down":
-                    nv.nvfp4_gemm(blk.s, W["down"], out, blk.x1, stream)
+                    nv.nvfp4_gemm(blk.s, W["down"], out, blk.x1, stream, blk.ws_gemm)
                 elif args.only == "qkv":
-                    nv.nvfp4_gemm(blk.h, W["qkv"], blk.qkv, None, stream)
+                    nv.nvfp4_gemm(blk.h, W["qkv"], blk.qkv, None, stream, blk.ws_gemm)
                 elif args.only == "norm_quantize":
                     nv.nvfp4_quantize(x, blk.h.g, blk.h, blk.attn_norm, 1e-6, None, stream)
                 elif args.only == "step":

@@ -99,10 +99,18 @@ size_t nvfp4_codes_bytes(int64_t rows, int64_t cols);
 size_t nvfp4_sf_bytes(int64_t rows, int64_t cols);
 /* Workspace of nvfp4_amax_scale (8 bytes, 256-B aligned). */
 size_t nvfp4_amax_workspace_bytes(void);
+/* Workspace that lets nvfp4_gemm split its work evenly over all SMs of the
+ * current device (8 KB of ready flags + 128 KB per SM; 0 when no device is
+ * usable). */
+size_t nvfp4_gemm_workspace_bytes(void);
 /* Workspace of nvfp4_gemm_swiglu for an A of T rows and an intermediate of I
- * columns: 256 bytes (STATIC) or 256 + T*I*2 bytes (DYNAMIC). */
+ * columns on the current device: 256 + 8192 bytes, + T*I*2 (DYNAMIC), + the
+ * split schedule's 128 KB per SM.  A workspace without the last part is
+ * accepted (the call then runs unsplit). */
 size_t nvfp4_swiglu_workspace_bytes(int64_t T, int64_t I, int inter_mode);
-/* Workspace of nvfp4_mlp (T tokens, hidden H, intermediate I). */
+/* Workspace of nvfp4_mlp (T tokens, hidden H, intermediate I) on the current
+ * device; likewise, its last 128 KB per SM (the split schedule's) may be
+ * left out. */
 size_t nvfp4_mlp_workspace_bytes(int64_t T, int64_t H, int64_t I, int inter_mode);
 /* Static description of a status code. */
 const char* nvfp4_status_string(int status);
@@ -166,11 +174,17 @@ int nvfp4_quantize(const void* x, int64_t rows, int64_t cols, int64_t ldx,
  *   A        activations, rows M = T (any M >= 1), cols K.
  *   W        weights [N x K] (K-major, as nn.Linear stores them).
  *   out      bf16 [M x N], pitch ldo; may alias residual (same pitch).
+ *   workspace NULL, or >= 8192 bytes, 256-B aligned, zero-filled once after
+ *            allocation (calls leave it zeroed); calls sharing one workspace
+ *            must be stream-ordered.  With nvfp4_gemm_workspace_bytes() bytes
+ *            the GEMM may split its tiles' K ranges over all SMs when whole
+ *            tiles would leave part of the GPU idle (fp32 partials combined
+ *            in the workspace); otherwise whole tiles are spread over the SMs.
  * Requires K == A->cols == W->cols, K % 64 == 0, N % 16 == 0.
  */
 int nvfp4_gemm(const nvfp4_tensor_t* A, const nvfp4_tensor_t* W,
                void* out, int64_t ldo, const void* residual, int64_t ldr,
-               nvfp4_stream_t stream);
+               void* workspace, size_t workspace_bytes, nvfp4_stream_t stream);
 
 /*
  * nvfp4_gemm_swiglu -- fused gate/up GEMM with SwiGLU epilogue and FP4

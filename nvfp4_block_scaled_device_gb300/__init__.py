@@ -39,6 +39,7 @@ _SIGS = {
     "nvfp4_codes_bytes": (ctypes.c_size_t, [ctypes.c_int64, ctypes.c_int64]),
     "nvfp4_sf_bytes": (ctypes.c_size_t, [ctypes.c_int64, ctypes.c_int64]),
     "nvfp4_amax_workspace_bytes": (ctypes.c_size_t, []),
+    "nvfp4_gemm_workspace_bytes": (ctypes.c_size_t, []),
     "nvfp4_swiglu_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int64, ctypes.c_int64, ctypes.c_int]),
     "nvfp4_mlp_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int]),
     "nvfp4_status_string": (ctypes.c_char_p, [ctypes.c_int]),
@@ -50,7 +51,8 @@ _SIGS = {
                                       ctypes.c_void_p, ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p,
                                       ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
     "nvfp4_gemm": (ctypes.c_int, [ctypes.POINTER(_TensorC), ctypes.POINTER(_TensorC), ctypes.c_void_p,
-                                  ctypes.c_int64, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p]),
+                                  ctypes.c_int64, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p,
+                                  ctypes.c_size_t, ctypes.c_void_p]),
     "nvfp4_gemm_swiglu": (ctypes.c_int, [ctypes.POINTER(_TensorC), ctypes.POINTER(_TensorC),
                                          ctypes.POINTER(_TensorC), ctypes.c_int, ctypes.c_void_p,
                                          ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
@@ -129,6 +131,10 @@ def amax_workspace_bytes() -> int:
     return int(lib().nvfp4_amax_workspace_bytes())
 
 
+def gemm_workspace_bytes() -> int:
+    return int(lib().nvfp4_gemm_workspace_bytes())
+
+
 def swiglu_workspace_bytes(T: int, I: int, inter_mode: int) -> int:
     return int(lib().nvfp4_swiglu_workspace_bytes(T, I, inter_mode))
 
@@ -197,12 +203,15 @@ def quantize_new(x: torch.Tensor, ws: torch.Tensor, norm_w=None, eps=1e-6, strea
     return t
 
 
-def nvfp4_gemm(A: NVFP4Tensor, W: NVFP4Tensor, out: torch.Tensor, residual=None, stream=None):
+def nvfp4_gemm(A: NVFP4Tensor, W: NVFP4Tensor, out: torch.Tensor, residual=None, stream=None, workspace=None):
+    """workspace: None, or a zero-filled uint8 tensor (see workspace()) of
+    gemm_workspace_bytes() bytes that lets the GEMM split tiles over all SMs."""
     _, _, ldo = _bf16_2d(out, "out")
     ldr = _bf16_2d(residual, "residual")[2] if residual is not None else 0
     a, w = A.c(), W.c()
+    nbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     _check(lib().nvfp4_gemm(ctypes.byref(a), ctypes.byref(w), _ptr(out), ldo, _ptr(residual), ldr,
-                            _stream(stream)), "nvfp4_gemm")
+                            _ptr(workspace), nbytes, _stream(stream)), "nvfp4_gemm")
 
 
 def nvfp4_gemm_swiglu(A: NVFP4Tensor, W_gate: NVFP4Tensor, W_up: NVFP4Tensor, inter_mode: int,

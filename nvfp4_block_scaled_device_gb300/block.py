@@ -27,7 +27,8 @@ from __future__ import annotations
 
 import torch
 
-from . import (NVFP4_INTER_DYNAMIC, NVFP4_INTER_STATIC, NVFP4Tensor, mlp_workspace_bytes, nvfp4_amax_scale,
+from . import (NVFP4_INTER_DYNAMIC, NVFP4_INTER_STATIC, NVFP4Tensor, gemm_workspace_bytes, mlp_workspace_bytes,
+               nvfp4_amax_scale,
                nvfp4_gemm, nvfp4_gemm_swiglu, nvfp4_mlp, nvfp4_quantize, swiglu_workspace_bytes, workspace)
 
 
@@ -51,6 +52,7 @@ class PrefillBlock:
         self.x1 = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
         self.g_inter = torch.ones((1,), dtype=torch.float32, device=dev)
         self.ws_amax = workspace(256, dev)
+        self.ws_gemm = workspace(gemm_workspace_bytes(), dev)   # split schedule of the plain GEMMs
         self.ws_mlp = workspace(mlp_workspace_bytes(T, H, I, NVFP4_INTER_DYNAMIC), dev)
         # buffers of the decomposed MLP (same kernels as nvfp4_mlp, with a
         # launch boundary exposed between them for per-kernel timing)
@@ -64,13 +66,13 @@ class PrefillBlock:
         nvfp4_amax_scale(x, self.h.g, self.ws_amax, self.attn_norm, self.eps, stream)
         nvfp4_quantize(x, self.h.g, self.h, self.attn_norm, self.eps, None, stream)
         rec("qkv0")
-        nvfp4_gemm(self.h, self.w["qkv"], self.qkv, None, stream)
+        nvfp4_gemm(self.h, self.w["qkv"], self.qkv, None, stream, self.ws_gemm)
         rec("qkv1")
         q = self.qkv[:, :self.H]
         nvfp4_amax_scale(q, self.a.g, self.ws_amax, None, self.eps, stream)
         nvfp4_quantize(q, self.a.g, self.a, None, self.eps, None, stream)
         rec("o0")
-        nvfp4_gemm(self.a, self.w["o"], self.x1, x, stream)
+        nvfp4_gemm(self.a, self.w["o"], self.x1, x, stream, self.ws_gemm)
         rec("o1")
 
     def calibrate(self, x: torch.Tensor, out: torch.Tensor, stream=None):
@@ -98,7 +100,7 @@ class PrefillBlock:
         nvfp4_gemm_swiglu(self.hm, self.w["gate"], self.w["up"], NVFP4_INTER_STATIC, self.g_inter, self.s,
                           self.ws_swiglu, None, stream)
         rec("gu1")
-        nvfp4_gemm(self.s, self.w["down"], out, self.x1, stream)
+        nvfp4_gemm(self.s, self.w["down"], out, self.x1, stream, self.ws_gemm)
         rec("dn1")
 
     EVENT_NAMES = ("qkv0", "qkv1", "o0", "o1", "mlp0", "gu0", "gu1", "dn1")

@@ -149,9 +149,28 @@ cudaError_t run_gemm(const CUtensorMap& ma, const CUtensorMap& mb0, const CUtens
 }
 
 // Shared by nvfp4_gemm_swiglu and nvfp4_mlp.
+// Split-schedule scratch of one call: the flag block and, when the
+// workspace has room for one slot per SM, the partial slots (else nullptr:
+// no split).
+struct SplitScratch {
+    int* flags = nullptr;
+    float* partials = nullptr;
+};
+
+SplitScratch split_scratch(const DeviceInfo* d, uint8_t* flags, uint8_t* partials, size_t partial_room)
+{
+    SplitScratch sp;
+    if (d->num_sms <= kSplitMaxCtas && partial_room >= split_partial_bytes(d->num_sms)) {
+        sp.flags = reinterpret_cast<int*>(flags);
+        sp.partials = reinterpret_cast<float*>(partials);
+    }
+    return sp;
+}
+
 int run_swiglu(const DeviceInfo* d, const nvfp4_tensor_t* A, const nvfp4_tensor_t* Wg, const nvfp4_tensor_t* Wu,
                int mode, float* g_inter, uint8_t* s_codes, int64_t ld_s_codes, uint8_t* s_sf,
-               __nv_bfloat16* s_bf16_user, uint8_t* ws, cudaStream_t stream)
+               __nv_bfloat16* s_bf16_user, uint32_t* amax_ws, __nv_bfloat16* s_bf16_scratch, SplitScratch split,
+               cudaStream_t stream)
 {
     const int64_t T = A->rows, I = Wg->rows;
     CUtensorMap ma, mg, mu;
@@ -175,7 +194,8 @@ int run_swiglu(const DeviceInfo* d, const nvfp4_tensor_t* A, const nvfp4_tensor_
     a.ld_s_codes = ld_s_codes;
     a.s_sf = s_sf;
     a.s_kb_pad = pad_to(I / 16, 4);
-    uint32_t* amax_ws = reinterpret_cast<uint32_t*>(ws);
+    a.sk_flags = split.flags;
+    a.sk_partials = split.partials;
     if (mode == NVFP4_INTER_STATIC) {
         a.epilogue = kEpiSwigluFp4;
         a.g_inter = g_inter;
@@ -183,7 +203,7 @@ int run_swiglu(const DeviceInfo* d, const nvfp4_tensor_t* A, const nvfp4_tensor_
         a.ld_s = I;
         NVFP4_CUDA(run_gemm(ma, mg, mu, a, d, stream));
     } else {
-        __nv_bfloat16* s_bf16 = s_bf16_user ? s_bf16_user : reinterpret_cast<__nv_bfloat16*>(ws + 256);
+        __nv_bfloat16* s_bf16 = s_bf16_user ? s_bf16_user : s_bf16_scratch;
         a.epilogue = kEpiSwigluBf16;
         a.s_bf16 = s_bf16;
         a.ld_s = I;
@@ -210,7 +230,46 @@ int check_swiglu_args(const nvfp4_tensor_t* A, const nvfp4_tensor_t* Wg, const n
     return NVFP4_OK;
 }
 
+// SMs of the current device (0 without a usable device): the split
+// schedule's partial slots in the workspace sizes are one per SM.
+int current_device_sms()
+{
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return sms <= kSplitMaxCtas ? sms : 0;
+}
+
 }  // namespace
+
+// Workspace layouts (all offsets 256-B aligned).  Without the trailing
+// partial slots a call still runs, unsplit.
+//   swiglu: [256 amax words][split flags][DYNAMIC: bf16 T x I][partials]
+//   mlp:    [256 amax words][split flags][h codes][h scales][s codes]
+//           [s scales][DYNAMIC: bf16 T x I][partials]
+size_t nvfp4::swiglu_base_workspace_bytes(int64_t T, int64_t I, int inter_mode)
+{
+    size_t b = 256 + kSplitFlagBytes;
+    if (inter_mode == NVFP4_INTER_DYNAMIC) b += align256((size_t)T * (size_t)I * 2);
+    return b;
+}
+
+size_t nvfp4::mlp_base_workspace_bytes(int64_t T, int64_t H, int64_t I, int inter_mode)
+{
+    size_t b = 256 + kSplitFlagBytes;                 // amax words, split flags
+    b += align256(nvfp4_codes_bytes(T, H));           // h codes
+    b += align256(nvfp4_sf_bytes(T, H));              // h scales
+    b += align256(nvfp4_codes_bytes(T, I));           // s codes
+    b += align256(nvfp4_sf_bytes(T, I));              // s scales
+    if (inter_mode == NVFP4_INTER_DYNAMIC) b += align256((size_t)T * (size_t)I * 2);
+    return b;
+}
 
 extern "C" {
 
@@ -228,22 +287,16 @@ size_t nvfp4_sf_bytes(int64_t rows, int64_t cols)
 
 size_t nvfp4_amax_workspace_bytes(void) { return kAmaxWorkspaceBytes; }
 
+size_t nvfp4_gemm_workspace_bytes(void) { return kSplitFlagBytes + split_partial_bytes(current_device_sms()); }
+
 size_t nvfp4_swiglu_workspace_bytes(int64_t T, int64_t I, int inter_mode)
 {
-    size_t b = 256;
-    if (inter_mode == NVFP4_INTER_DYNAMIC) b += align256((size_t)T * (size_t)I * 2);
-    return b;
+    return nvfp4::swiglu_base_workspace_bytes(T, I, inter_mode) + split_partial_bytes(current_device_sms());
 }
 
 size_t nvfp4_mlp_workspace_bytes(int64_t T, int64_t H, int64_t I, int inter_mode)
 {
-    size_t b = 256;                                   // amax words
-    b += align256(nvfp4_codes_bytes(T, H));           // h codes
-    b += align256(nvfp4_sf_bytes(T, H));              // h scales
-    b += align256(nvfp4_codes_bytes(T, I));           // s codes
-    b += align256(nvfp4_sf_bytes(T, I));              // s scales
-    b += nvfp4_swiglu_workspace_bytes(T, I, inter_mode);
-    return b;
+    return nvfp4::mlp_base_workspace_bytes(T, H, I, inter_mode) + split_partial_bytes(current_device_sms());
 }
 
 const char* nvfp4_status_string(int status)
@@ -309,13 +362,15 @@ int nvfp4_quantize(const void* x, int64_t rows, int64_t cols, int64_t ldx, const
 }
 
 int nvfp4_gemm(const nvfp4_tensor_t* A, const nvfp4_tensor_t* W, void* out, int64_t ldo, const void* residual,
-               int64_t ldr, nvfp4_stream_t stream)
+               int64_t ldr, void* workspace, size_t workspace_bytes, nvfp4_stream_t stream)
 {
     NVFP4_TRY(check_tensor(A));
     NVFP4_TRY(check_tensor(W));
     if (A->cols != W->cols || W->rows % 16 != 0) return NVFP4_ERR_INVALID_ARG;
     NVFP4_TRY(check_bf16_matrix(out, A->rows, W->rows, ldo));
     if (residual) NVFP4_TRY(check_bf16_matrix(residual, A->rows, W->rows, ldr));
+    if (workspace && workspace_bytes < kSplitFlagBytes) return NVFP4_ERR_WORKSPACE;
+    if (workspace && !aligned(workspace, 256)) return NVFP4_ERR_MISALIGNED;
     DeviceInfo* d = nullptr;
     NVFP4_TRY(device_info(&d));
     NVFP4_TRY(encoder());
@@ -338,6 +393,13 @@ int nvfp4_gemm(const nvfp4_tensor_t* A, const nvfp4_tensor_t* W, void* out, int6
     a.residual = static_cast<const __nv_bfloat16*>(residual);
     a.ldr = ldr;
     a.status = d->status;
+    if (workspace) {
+        uint8_t* ws = static_cast<uint8_t*>(workspace);
+        const SplitScratch sp =
+            split_scratch(d, ws, ws + kSplitFlagBytes, workspace_bytes - kSplitFlagBytes);
+        a.sk_flags = sp.flags;
+        a.sk_partials = sp.partials;
+    }
     NVFP4_CUDA(run_gemm(ma, mb, mb, a, d, (cudaStream_t)stream));
     return NVFP4_OK;
 }
@@ -351,13 +413,17 @@ int nvfp4_gemm_swiglu(const nvfp4_tensor_t* A, const nvfp4_tensor_t* W_gate, con
     if (!s_codes || !s_sf || ld_s_codes < I / 2) return NVFP4_ERR_INVALID_ARG;
     if (!aligned(s_codes, 16) || ld_s_codes % 16 != 0 || !aligned(s_sf, 128)) return NVFP4_ERR_MISALIGNED;
     if (s_bf16 && !aligned(s_bf16, 16)) return NVFP4_ERR_MISALIGNED;
-    if (!workspace || workspace_bytes < nvfp4_swiglu_workspace_bytes(T, I, inter_mode)) return NVFP4_ERR_WORKSPACE;
+    const size_t base = swiglu_base_workspace_bytes(T, I, inter_mode);
+    if (!workspace || workspace_bytes < base) return NVFP4_ERR_WORKSPACE;
     if (!aligned(workspace, 256)) return NVFP4_ERR_MISALIGNED;
     DeviceInfo* d = nullptr;
     NVFP4_TRY(device_info(&d));
     NVFP4_TRY(encoder());
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
     return run_swiglu(d, A, W_gate, W_up, inter_mode, g_inter, s_codes, ld_s_codes, s_sf,
-                      static_cast<__nv_bfloat16*>(s_bf16), static_cast<uint8_t*>(workspace), (cudaStream_t)stream);
+                      static_cast<__nv_bfloat16*>(s_bf16), reinterpret_cast<uint32_t*>(ws),
+                      reinterpret_cast<__nv_bfloat16*>(ws + 256 + kSplitFlagBytes),
+                      split_scratch(d, ws + 256, ws + base, workspace_bytes - base), (cudaStream_t)stream);
 }
 
 int nvfp4_mlp(const void* x, int64_t T, int64_t H, int64_t ldx, const void* norm_w, float eps,
@@ -379,7 +445,8 @@ int nvfp4_mlp(const void* x, int64_t T, int64_t H, int64_t ldx, const void* norm
     if (!g_inter) return NVFP4_ERR_INVALID_ARG;
     NVFP4_TRY(check_bf16_matrix(out, T, H, ldo));
     if (add_residual && out == x && ldo != ldx) return NVFP4_ERR_INVALID_ARG;
-    if (!workspace || workspace_bytes < nvfp4_mlp_workspace_bytes(T, H, I, inter_mode)) return NVFP4_ERR_WORKSPACE;
+    const size_t base = mlp_base_workspace_bytes(T, H, I, inter_mode);
+    if (!workspace || workspace_bytes < base) return NVFP4_ERR_WORKSPACE;
     if (!aligned(workspace, 256)) return NVFP4_ERR_MISALIGNED;
     DeviceInfo* d = nullptr;
     NVFP4_TRY(device_info(&d));
@@ -389,7 +456,8 @@ int nvfp4_mlp(const void* x, int64_t T, int64_t H, int64_t ldx, const void* norm
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     uint32_t* amax_ws = reinterpret_cast<uint32_t*>(ws);          // words [0,2)
     float* g_h = reinterpret_cast<float*>(ws + 64);
-    size_t off = 256;
+    const SplitScratch split = split_scratch(d, ws + 256, ws + base, workspace_bytes - base);
+    size_t off = 256 + kSplitFlagBytes;
     uint8_t* h_codes = ws + off;
     off += align256(nvfp4_codes_bytes(T, H));
     uint8_t* h_sf = ws + off;
@@ -398,7 +466,7 @@ int nvfp4_mlp(const void* x, int64_t T, int64_t H, int64_t ldx, const void* norm
     off += align256(nvfp4_codes_bytes(T, I));
     uint8_t* s_sf = ws + off;
     off += align256(nvfp4_sf_bytes(T, I));
-    uint8_t* swiglu_ws = ws + off;
+    __nv_bfloat16* s_bf16_scratch = reinterpret_cast<__nv_bfloat16*>(ws + off);   // DYNAMIC only
 
     const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
     const __nv_bfloat16* nw = static_cast<const __nv_bfloat16*>(norm_w);
@@ -407,7 +475,10 @@ int nvfp4_mlp(const void* x, int64_t T, int64_t H, int64_t ldx, const void* norm
     NVFP4_CUDA(launch_quantize(xb, T, H, ldx, nw, eps, g_h, h_codes, H / 2, h_sf, nullptr, d->num_sms, st));
     // 3: fused gate/up GEMM + SwiGLU + FP4 requant
     const nvfp4_tensor_t h = {h_codes, h_sf, g_h, T, H, H / 2};
-    NVFP4_TRY(run_swiglu(d, &h, W_gate, W_up, inter_mode, g_inter, s_codes, I / 2, s_sf, nullptr, swiglu_ws, st));
+    // the gate/up kernel and the down kernel run one after the other on the
+    // stream, so they share the split scratch
+    NVFP4_TRY(run_swiglu(d, &h, W_gate, W_up, inter_mode, g_inter, s_codes, I / 2, s_sf, nullptr, amax_ws,
+                         s_bf16_scratch, split, st));
     // 4: down GEMM (+ residual)
     const nvfp4_tensor_t s = {s_codes, s_sf, g_inter, T, I, I / 2};
     CUtensorMap ma, mb;
@@ -429,6 +500,8 @@ int nvfp4_mlp(const void* x, int64_t T, int64_t H, int64_t ldx, const void* norm
     a.residual = add_residual ? xb : nullptr;
     a.ldr = ldx;
     a.status = d->status;
+    a.sk_flags = split.flags;
+    a.sk_partials = split.partials;
     NVFP4_CUDA(run_gemm(ma, mb, mb, a, d, st));
     return NVFP4_OK;
 }

@@ -23,8 +23,12 @@
 //   warps 8-15  epilogue: drain the accumulator to registers, release it to
 //               the MMA warp, then scale / SwiGLU / requantize / store while
 //               the next tile accumulates.
-// Persistent: grid = min(#tiles, #SMs); tile t -> (m = t % Mt, n = t / Mt),
-// so CTAs running together share the same weight tiles through L2.
+// Persistent: grid = min(#tiles, #SMs), tile t -> (m = t % Mt, n = t / Mt),
+// so CTAs running together share the same weight tiles through L2; or, for
+// deep-K tiles whose last wave would leave more than a tenth of the GPU
+// idle, a split schedule over all SMs (stream-K: each CTA an equal run of
+// the flattened (tile, K stage) units; a tile's CTAs combine fp32 partials
+// through a workspace, the one holding its first K stage finishing it).
 #include "common.cuh"
 #include "gemm_epilogue.cuh"
 #include "internal.h"
@@ -71,15 +75,28 @@ static_assert(kProducers == kEpiWarp0 - 1, "producers: warpgroups 0-1 less the M
 constexpr uint32_t kIdesc = (1u << 7) | (1u << 10) | ((256u >> 3) << 17) | ((128u >> 4) << 24);
 
 #ifdef NVFP4_TRACE
-// Debug timeline of CTA 0 (built only with -DNVFP4_TRACE): SM clock at each
+// Debug timeline of CTA NVFP4_TRACE_CTA (default 0; built only with
+// -DNVFP4_TRACE): SM clock at each
 // pipeline handoff.  [0,256) producer empty-wait done, [256,512) producer
 // issued, [512,768) MMA full-wait done, [768,1024) MMA issued, [1024,1088)
-// MMA acc-empty done, [1088,1152) epilogue acc-full done, [1152,1216) drained.
-__device__ unsigned long long g_trace[1216];
+// MMA acc-empty done, [1088,1152) epilogue acc-full done, [1152,1216) drained,
+// [1216,1280) split partials added (or partial stored).
+__device__ unsigned long long g_trace[1280];
+#ifndef NVFP4_TRACE_CTA
+#define NVFP4_TRACE_CTA 0
+#endif
 #define TRACE(slot, i) \
-    do { if (blockIdx.x == 0 && (i) < 64 * ((slot) < 1024 ? 4 : 1)) g_trace[(slot) + (i)] = clock64(); } while (0)
+    do { if (blockIdx.x == NVFP4_TRACE_CTA && (i) < 64 * ((slot) < 1024 ? 4 : 1)) g_trace[(slot) + (i)] = clock64(); } while (0)
+// Per-CTA events on the global timer (ns): [c][0] start, [c][1] first
+// accumulator ready, [c][2] first segment's partial stored or tile
+// finished, [c][3] last segment finished.
+__device__ unsigned long long g_trace_cta[256][4];
+__device__ unsigned long long g_trace_fix[16];   // CTA 0, first epilogue warp: each contributor's flag seen
+#define TRACE_CTA(k) \
+    do { if (blockIdx.x < 256) g_trace_cta[blockIdx.x][k] = globaltimer(); } while (0)
 #else
 #define TRACE(slot, i) do { } while (0)
+#define TRACE_CTA(k) do { } while (0)
 #endif
 
 struct Ctrl {
@@ -93,6 +110,99 @@ struct Ctrl {
 };
 static_assert(sizeof(Ctrl) <= kCtrlBytes, "control block");
 
+// Work schedule of one CTA, walked as segments (tile, first K stage, end K
+// stage) by every role alike: whole tiles strided over the grid, or (split)
+// a contiguous range of the flattened (tile, K stage) units, CTA c taking
+// units [c*U/G, (c+1)*U/G) of U = tiles x stages on a grid of G CTAs.
+struct Schedule {
+    int64_t next;     // whole tiles: next tile; split: next unit
+    int64_t end;      // split: end of this CTA's units
+    int64_t tiles;
+    int stages;       // K stages per tile
+    bool split;
+};
+
+__device__ __forceinline__ int64_t split_first_unit(int64_t cta, int64_t units)
+{
+    return cta * units / gridDim.x;
+}
+
+__device__ __forceinline__ Schedule make_schedule(int64_t tiles, int stages, bool split)
+{
+    Schedule sc;
+    sc.tiles = tiles;
+    sc.stages = stages;
+    sc.split = split;
+    if (split) {
+        sc.next = split_first_unit(blockIdx.x, tiles * stages);
+        sc.end = split_first_unit(blockIdx.x + 1, tiles * stages);
+    } else {
+        sc.next = blockIdx.x;
+        sc.end = 0;
+    }
+    return sc;
+}
+
+__device__ __forceinline__ bool next_segment(Schedule& sc, int64_t& tile, int& ks, int& ke)
+{
+    if (!sc.split) {
+        if (sc.next >= sc.tiles) return false;
+        tile = sc.next;
+        ks = 0;
+        ke = sc.stages;
+        sc.next += gridDim.x;
+        return true;
+    }
+    if (sc.next >= sc.end) return false;
+    tile = sc.next / sc.stages;
+    ks = (int)(sc.next - tile * sc.stages);
+    const int64_t left = sc.end - sc.next;
+    ke = left < sc.stages - ks ? ks + (int)left : sc.stages;
+    sc.next += ke - ks;
+    return true;
+}
+
+// Ready flag of a partial accumulator: set with release semantics after the
+// slot's stores, read with acquire semantics before its loads.
+__device__ __forceinline__ void flag_set_release(int* f, int v)
+{
+    asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(f), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ int flag_get_relaxed(const int* f)
+{
+    int v;
+    asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
+    return v;
+}
+
+// Warp-wide bounded wait (converged: every lane polls, a vote decides) for a
+// ready flag; gives up like mbar_wait_warp.  The polls are relaxed: the
+// caller orders its reads of the flagged data after the wait with one
+// acquire fence.
+__device__ __forceinline__ bool flag_wait_warp(const int* f, volatile int* abort_flag, int* status, int site)
+{
+    const uint64_t t0 = clock64();
+    for (uint32_t i = 0;; i++) {
+        if (__all_sync(0xffffffffu, flag_get_relaxed(f) != 0)) return true;
+        if ((i & 255u) == 255u) {
+            int stop = *abort_flag ? 1 : ((uint64_t)(clock64() - t0) > kWaitLimitCycles ? 2 : 0);
+            stop = __shfl_sync(0xffffffffu, stop, 0);
+            if (stop != 0) {
+                if (stop == 2 && (threadIdx.x & 31) == 0) {
+                    *abort_flag = 1;
+                    if (status) atomicCAS(status, 0, kErrTimeout * 100 + site);
+                }
+                __syncwarp();
+                return false;
+            }
+        }
+    }
+}
+
+// kSplit: the split schedule (its fix-up code is compiled into this
+// instantiation only; the whole-tile instantiation carries none of it).
+template <bool kSplit>
 __global__ void __launch_bounds__(kNumThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b0,
                 const __grid_constant__ CUtensorMap map_b1, const GemmArgs args)
@@ -115,6 +225,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     const int num_kstages = (num_kk + 3) / 4;
     const int full_kstages = num_kk / 4;       // stages of 4 K-steps
     const int tail_kk = num_kk % 4;            // K-steps of a last, partial stage
+    constexpr bool split = kSplit;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; s++) {
@@ -140,6 +251,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = ctrl->tmem_base;
+    if (threadIdx.x == 0) TRACE_CTA(0);
 
     if (warp < kEpiWarp0) {
         // warpgroups 0-1: one register-budget instruction for all eight warps
@@ -169,7 +281,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             uint32_t ph = 0, issued = 0, issued_ph = 0;
             int kcount = 0;
             bool ok = true;
-            for (int64_t tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+            Schedule sched = make_schedule(num_tiles, num_kstages, split);
+            int64_t tile;
+            int ks, ke;
+            while (ok && next_segment(sched, tile, ks, ke)) {
                 const int64_t mt = tile % num_m, nt = tile / num_m;
                 const int32_t ya = (int32_t)(mt * 128);
                 int32_t yb0, yb1;
@@ -194,8 +309,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 const uint32_t code_bytes =
                     kBox * (1u + (ya + kCodeBoxRows < args.M ? 1u : 0u) + 1u + (yb0 + kCodeBoxRows < args.N ? 1u : 0u) +
                             (yb1 < args.N ? 1u : 0u) + (yb1 + kCodeBoxRows < args.N ? 1u : 0u));
-                const uint8_t* pa = args.sfa + mt * args.sfa_tile_stride;
-                for (int kb = 0; kb < num_kstages; kb++) {
+                const uint8_t* pa = args.sfa + mt * args.sfa_tile_stride + (size_t)ks * 4 * kSfTile;
+                pb0 += (size_t)ks * 4 * kSfTile;
+                pb1 += (size_t)ks * 4 * kSfTile;
+                for (int kb = ks; kb < ke; kb++) {
                     if (!mbar_wait_warp(empty0 + 8u * (uint32_t)s, ph ^ 1u, abort_flag, args.status, 1)) {
                         ok = false;
                         break;
@@ -254,13 +371,18 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             uint32_t ph = 0, acc_ph = 0;
             bool ok = true;
             int kcount = 0, tcount = 0;
-            for (int64_t tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+            Schedule sched = make_schedule(num_tiles, num_kstages, split);
+            int64_t tile;
+            int ks, ke;
+            while (ok && next_segment(sched, tile, ks, ke)) {
                 if (!mbar_wait_warp(smem_u32(&ctrl->acc_empty), acc_ph ^ 1u, abort_flag, args.status, 2)) break;
                 TRACE(1024, tcount);
                 tcount++;
                 tc_fence_after();
-                // full stages: nothing but the wait and one fused issue block
-                for (int kb = 0; kb < full_kstages; kb++) {
+                // full stages of the segment: nothing but the wait and one
+                // fused issue block
+                const int kfull_end = ke < full_kstages ? ke : full_kstages;
+                for (int kb = ks; kb < kfull_end; kb++) {
                     if (!mbar_wait_warp(full0 + 8u * (uint32_t)s, ph, abort_flag, args.status, 3)) {
                         ok = false;
                         break;
@@ -271,7 +393,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     const uint32_t soff = (uint32_t)s * (kStageBytes >> 4);
                     const uint32_t a_lo = desc_a_lo + soff;
                     stage_issue_1sm(tmem, tmem + kAccCols + (uint32_t)s * kSfColsPerStage, desc_sf_lo + soff,
-                                    desc_sf_hi, a_lo, a_lo + (kABytes >> 4), desc_sw_hi, kIdesc, kb != 0 ? 1u : 0u,
+                                    desc_sf_hi, a_lo, a_lo + (kABytes >> 4), desc_sw_hi, kIdesc, kb != ks ? 1u : 0u,
                                     empty0 + 8u * (uint32_t)s);
                     TRACE(768, kcount);
                     kcount++;
@@ -280,7 +402,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                         ph ^= 1u;
                     }
                 }
-                if (ok && tail_kk != 0) {
+                if (ok && ke > full_kstages) {
                     // K tail: a last stage of fewer than 4 K-steps
                     if (!mbar_wait_warp(full0 + 8u * (uint32_t)s, ph, abort_flag, args.status, 3)) {
                         ok = false;
@@ -302,7 +424,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                             const uint32_t c = sf_stage + (uint32_t)kk * kSfColsPerKK;
                             mma_mxf4nvf4_warp(tmem, desc_from(a_lo + 2u * kk, desc_sw_hi),
                                               desc_from(b_lo + 2u * kk, desc_sw_hi), kIdesc, c, c + 4,
-                                              (full_kstages | kk) != 0 ? 1u : 0u);
+                                              (full_kstages != ks || kk != 0) ? 1u : 0u);
                         }
                         mma_commit_warp(empty0 + 8u * (uint32_t)s);
                         kcount++;
@@ -334,10 +456,15 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         uint32_t acc_ph = 0;
         float wamax = 0.0f;
         int ecount = 0;
-        for (int64_t tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+        const int we = warp - kEpiWarp0;   // epilogue warp index (its slice of a partial slot)
+        Schedule sched = make_schedule(num_tiles, num_kstages, split);
+        int64_t tile;
+        int ks, ke;
+        while (next_segment(sched, tile, ks, ke)) {
             const int64_t mt = tile % num_m, nt = tile / num_m;
             if (!mbar_wait_warp<true>(smem_u32(&ctrl->acc_full), acc_ph, abort_flag, args.status, 4)) break;
             if (warp == kEpiWarp0 && lane == 0) TRACE(1088, ecount);
+            if (warp == kEpiWarp0 && lane == 0 && ecount == 0) TRACE_CTA(1);
             tc_fence_after();
             float v[128];
             if (!swiglu) {
@@ -360,7 +487,69 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             acc_ph ^= 1u;
 
             const int64_t row = mt * 128 + q * 32 + lane;
+            if (split && ks != 0) {
+                // later K stages of a tile finished by another CTA: this
+                // warp's 32 x 128 partial into the CTA's slot (values 4j..4j+3
+                // of lane l as one 16-byte vector at [we][j][l]: each store
+                // instruction of the warp writes 512 contiguous bytes), then
+                // its ready flag
+                float4* slot = reinterpret_cast<float4*>(args.sk_partials + (int64_t)blockIdx.x * kSplitSlotFloats) +
+                               we * 1024 + lane;
+                if (row < args.M) {
+#pragma unroll
+                    for (int j = 0; j < 32; j++)
+                        __stcg(slot + j * 32, make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
+                }
+                // the warp's stores, ordered by __syncwarp before lane 0's
+                // release store of the flag, are visible to whoever acquires it
+                __syncwarp();
+                if (lane == 0) flag_set_release(args.sk_flags + blockIdx.x * kSplitFlagsPerCta + we, 1);
+                if (warp == kEpiWarp0 && lane == 0) TRACE(1216, ecount - 1);
+                if (warp == kEpiWarp0 && lane == 0) TRACE_CTA(2);
+                continue;
+            }
+            if (split && ke != num_kstages) {
+                // first K stages of a tile whose later stages other CTAs
+                // hold (each as the first segment of its range): wait for
+                // their partials, add them, then return their flags to zero
+                const int64_t units = num_tiles * num_kstages, tile_end = (tile + 1) * num_kstages;
+                int64_t c_end = (int64_t)blockIdx.x + 1;
+                while (c_end < (int64_t)gridDim.x && split_first_unit(c_end, units) < tile_end) c_end++;
+                bool got = true;
+                for (int64_t c = (int64_t)blockIdx.x + 1; c < c_end && got; c++) {
+                    got = flag_wait_warp(args.sk_flags + c * kSplitFlagsPerCta + we, abort_flag, args.status, 5);
+#ifdef NVFP4_TRACE
+                    if (blockIdx.x == 0 && warp == kEpiWarp0 && lane == 0 && c < 16) g_trace_fix[c] = globaltimer();
+#endif
+                }
+                if (!got) break;
+                asm volatile("fence.acq_rel.gpu;" ::: "memory");
+                if (row < args.M) {
+                    for (int64_t c = (int64_t)blockIdx.x + 1; c < c_end; c++) {
+                        const float4* slot =
+                            reinterpret_cast<const float4*>(args.sk_partials + c * kSplitSlotFloats) + we * 1024 + lane;
+#pragma unroll
+                        for (int jb = 0; jb < 32; jb += 16) {   // 16 loads in flight, then their adds
+                            float4 t[16];
+#pragma unroll
+                            for (int j = 0; j < 16; j++) t[j] = __ldcg(slot + (jb + j) * 32);
+#pragma unroll
+                            for (int j = 0; j < 16; j++) {
+                                v[4 * (jb + j)] += t[j].x;
+                                v[4 * (jb + j) + 1] += t[j].y;
+                                v[4 * (jb + j) + 2] += t[j].z;
+                                v[4 * (jb + j) + 3] += t[j].w;
+                            }
+                        }
+                    }
+                }
+                __syncwarp();
+                if (lane == 0)
+                    for (int64_t c = (int64_t)blockIdx.x + 1; c < c_end; c++) args.sk_flags[c * kSplitFlagsPerCta + we] = 0;
+                if (warp == kEpiWarp0 && lane == 0) TRACE(1216, ecount - 1);
+            }
             epilogue_row(args, swiglu, v, row, nt, h, alpha0, alpha1, g_inter, wamax);
+            if (warp == kEpiWarp0 && lane == 0) TRACE_CTA(3);
         }
         if (args.epilogue == kEpiSwigluBf16) {
 #pragma unroll
@@ -390,7 +579,9 @@ cudaError_t launch_gemm(const CUtensorMap& map_a, const CUtensorMap& map_b0, con
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 64 && !attr_set_for_device[dev]) {
-        e = cudaFuncSetAttribute(gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        e = cudaFuncSetAttribute(gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
         if (e != cudaSuccess) return e;
         attr_set_for_device[dev] = 1;
     }
@@ -398,17 +589,38 @@ cudaError_t launch_gemm(const CUtensorMap& map_a, const CUtensorMap& map_b0, con
     const int64_t num_m = (args.M + 127) / 128;
     const int64_t num_n = swiglu ? args.N / 128 : (args.N + 255) / 256;
     const int64_t tiles = num_m * num_n;
-    const unsigned grid = (unsigned)(tiles < num_sms ? tiles : num_sms);
-    gemm_kernel<<<grid, kNumThreads, kSmemBytes, stream>>>(map_a, map_b0, map_b1, args);
+    const int64_t stages = (args.K / 64 + 3) / 4;
+    // Whole tiles strided over min(tiles, SMs) CTAs, unless their last wave
+    // leaves more than a tenth of the GPU idle and the tiles are deep in K:
+    // then (given a workspace) every SM takes an equal share of the (tile,
+    // K stage) units.  A tile split over CTAs costs its finishing CTA a few
+    // microseconds of partial reads, which only deep tiles (>= 32 stages,
+    // K >= 8192) repay; spreading shallow tiles over all SMs also makes
+    // every CTA stream its own weight slab, which defeats the L2 sharing of
+    // concurrently running whole tiles.
+    const int64_t waves = (tiles + num_sms - 1) / num_sms;
+    const bool split = args.sk_partials != nullptr && args.sk_flags != nullptr && num_sms <= kSplitMaxCtas &&
+                       tiles * stages >= num_sms && tiles * 10 < waves * num_sms * 9 && stages >= 32;
+    if (split)
+        gemm_kernel<true><<<(unsigned)num_sms, kNumThreads, kSmemBytes, stream>>>(map_a, map_b0, map_b1, args);
+    else
+        gemm_kernel<false><<<(unsigned)(tiles < num_sms ? tiles : num_sms), kNumThreads, kSmemBytes, stream>>>(
+            map_a, map_b0, map_b1, args);
     return cudaGetLastError();
 }
 
 }  // namespace nvfp4
 
 #ifdef NVFP4_TRACE
+extern "C" int nvfp4_debug_trace_ctas(unsigned long long* out)
+{
+    if (cudaMemcpyFromSymbol(out, nvfp4::g_trace_cta, sizeof(nvfp4::g_trace_cta)) != cudaSuccess) return 4;
+    return cudaMemcpyFromSymbol(out + 1024, nvfp4::g_trace_fix, sizeof(nvfp4::g_trace_fix)) == cudaSuccess ? 0 : 4;
+}
+
 extern "C" int nvfp4_debug_trace(unsigned long long* out, int n)
 {
-    if (n > 1216) n = 1216;
+    if (n > 1280) n = 1280;
     return cudaMemcpyFromSymbol(out, nvfp4::g_trace, n * sizeof(unsigned long long)) == cudaSuccess ? 0 : 4;
 }
 #endif

@@ -68,7 +68,26 @@ struct GemmArgs {
     int64_t ld_s;
     uint32_t* amax_ws;
     int* status;
+    // split schedule (1-SM kernel): sk_partials (slots for at least as many
+    // CTAs as the device has SMs) and sk_flags set = the launcher may split
+    // (it then launches the split instantiation of the kernel).  Each CTA
+    // then takes a contiguous range of the flattened (tile, K stage) units;
+    // a tile split between CTAs is finished by the CTA holding its first K
+    // stage, from the others' partial accumulators (one fp32 slot of
+    // kSplitSlotFloats per CTA) and per-warp ready flags.
+    float* sk_partials;
+    int* sk_flags;
 };
+
+// Split-schedule workspace: a fixed block of ready flags (one per epilogue
+// warp of up to kSplitMaxCtas CTAs; zero before first use, and every
+// completed launch leaves them zero), and one 128 x 256 fp32 accumulator
+// slot per CTA of the launch.
+constexpr int64_t kSplitSlotFloats = 128 * 256;
+constexpr int kSplitFlagsPerCta = 8;
+constexpr int kSplitMaxCtas = 256;
+constexpr size_t kSplitFlagBytes = (size_t)kSplitMaxCtas * kSplitFlagsPerCta * 4;   // 8 KB
+inline size_t split_partial_bytes(int ctas) { return (size_t)ctas * (size_t)kSplitSlotFloats * 4; }
 
 // maps: A [M x K/2 bytes], B0 and B1 (B1 only for SwiGLU) with a 128x128-byte
 // box and 128-byte swizzle.
@@ -83,5 +102,11 @@ cudaError_t launch_gemm2(const CUtensorMap& map_a, const CUtensorMap& map_b0, co
                          const GemmArgs& args, int num_sms, cudaStream_t stream);
 
 size_t gemm_smem_bytes();
+
+// Workspace of nvfp4_gemm_swiglu / nvfp4_mlp without the split schedule's
+// partial slots (the least a call accepts; it then runs unsplit).  The
+// public size helpers add the slots for the current device.
+size_t swiglu_base_workspace_bytes(int64_t T, int64_t I, int inter_mode);
+size_t mlp_base_workspace_bytes(int64_t T, int64_t H, int64_t I, int inter_mode);
 
 }  // namespace nvfp4

@@ -53,16 +53,19 @@ extern "C" int nvfp4_mlp_noalloc(const void* x, int64_t T, int64_t H, int64_t ld
 {
     if (!W_gate || T < 1) return NVFP4_ERR_INVALID_ARG;
     if (inter_mode != NVFP4_INTER_STATIC && inter_mode != NVFP4_INTER_DYNAMIC) return NVFP4_ERR_INVALID_ARG;
-    // the intermediates of this call must fit the fixed array
-    if (nvfp4_mlp_workspace_bytes(T, H, W_gate->rows, inter_mode) > kNoallocScratchBytes)
+    // the intermediates of this call must fit the fixed array (the split
+    // schedule's partial slots are used when they fit as well)
+    if (nvfp4::mlp_base_workspace_bytes(T, H, W_gate->rows, inter_mode) > kNoallocScratchBytes)
         return NVFP4_ERR_WORKSPACE;
     void* scratch = nullptr;
     const int st = scratch_address(&scratch);
     if (st != NVFP4_OK) return st;
-    // The array keeps whatever the previous call left.  The amax words at its
-    // start must be zero when a call begins (a completed call leaves them
-    // zero; a call that stopped early might not), so clear them first.
-    if (cudaMemsetAsync(scratch, 0, 256, (cudaStream_t)stream) != cudaSuccess) return NVFP4_ERR_CUDA;
+    // The array keeps whatever the previous call left.  The amax words and
+    // the split schedule's ready flags at its start must be zero when a call
+    // begins (a completed call leaves them zero; a call that stopped early
+    // might not), so clear them first.
+    if (cudaMemsetAsync(scratch, 0, 256 + nvfp4::kSplitFlagBytes, (cudaStream_t)stream) != cudaSuccess)
+        return NVFP4_ERR_CUDA;
     return nvfp4_mlp(x, T, H, ldx, norm_w, eps, W_gate, W_up, W_down, inter_mode, g_inter, out, ldo, add_residual,
                      scratch, kNoallocScratchBytes, stream);
 }

@@ -48,6 +48,7 @@ def test_size_helpers(L):
     assert nv.sf_bytes(129, 5120) == 256 * 320
     assert nv.sf_bytes(1, 17408) == 128 * 1088
     assert nv.amax_workspace_bytes() >= 8
+    assert nv.gemm_workspace_bytes() >= 8192            # ready flags (+ partial slots with a device)
     assert nv.swiglu_workspace_bytes(1024, 17408, nv.NVFP4_INTER_DYNAMIC) >= 1024 * 17408 * 2
     assert nv.mlp_workspace_bytes(1024, 5120, 17408, nv.NVFP4_INTER_STATIC) >= (
         1024 * 2560 + 1024 * 320 + 1024 * 8704 + 1024 * 1088)
@@ -63,19 +64,19 @@ def test_invalid_arguments_rejected_on_host(L):
     import nvfp4_block_scaled_device_gb300 as nv
     NULL = None
     # NULL tensors
-    assert L.nvfp4_gemm(NULL, NULL, NULL, 0, NULL, 0, NULL) == 1
+    assert L.nvfp4_gemm(NULL, NULL, NULL, 0, NULL, 0, NULL, 0, NULL) == 1
     # bad shapes: cols not a multiple of 64
     a = nv._TensorC(16, 128 * 16, 4, 16, 100, 64)
     w = nv._TensorC(16, 128 * 16, 4, 512, 100, 64)
-    assert L.nvfp4_gemm(ctypes.byref(a), ctypes.byref(w), 16, 512, NULL, 0, NULL) == 1
+    assert L.nvfp4_gemm(ctypes.byref(a), ctypes.byref(w), 16, 512, NULL, 0, NULL, 0, NULL) == 1
     # misaligned codes pointer
     a = nv._TensorC(17, 128 * 16, 4, 16, 256, 128)
     w = nv._TensorC(16, 128 * 16, 4, 512, 256, 128)
-    assert L.nvfp4_gemm(ctypes.byref(a), ctypes.byref(w), 16, 512, NULL, 0, NULL) == 2
+    assert L.nvfp4_gemm(ctypes.byref(a), ctypes.byref(w), 16, 512, NULL, 0, NULL, 0, NULL) == 2
     # K mismatch
     a = nv._TensorC(16, 128 * 16, 4, 16, 256, 128)
     w = nv._TensorC(16, 128 * 16, 4, 512, 512, 256)
-    assert L.nvfp4_gemm(ctypes.byref(a), ctypes.byref(w), 16, 512, NULL, 0, NULL) == 1
+    assert L.nvfp4_gemm(ctypes.byref(a), ctypes.byref(w), 16, 512, NULL, 0, NULL, 0, NULL) == 1
     # quantize: cols % 64
     assert L.nvfp4_quantize(16, 4, 32, 32, NULL, 1e-6, 16, 16, 16, 128, NULL, NULL) == 1
     # amax: missing workspace

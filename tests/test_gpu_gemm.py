@@ -27,7 +27,7 @@ def ws(nv):
     return nv.workspace(256)
 
 
-def run_case(nv, ws, M, N, K, seed, residual=False, a_outliers=False):
+def run_case(nv, ws, M, N, K, seed, residual=False, a_outliers=False, split=False):
     rng = np.random.default_rng(seed)
     if a_outliers:
         a = synthetic.student_t_outliers(rng, (M, K))
@@ -41,7 +41,8 @@ def run_case(nv, ws, M, N, K, seed, residual=False, a_outliers=False):
     assert_same_quant(W, wc, wsf, gw, "W")
     res_bits = synthetic.normal(rng, (M, N)) if residual else None
     out = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
-    nv.nvfp4_gemm(A, W, out, residual=None if res_bits is None else dev(res_bits))
+    gws = nv.workspace(nv.gemm_workspace_bytes()) if split else None
+    nv.nvfp4_gemm(A, W, out, residual=None if res_bits is None else dev(res_bits), workspace=gws)
     torch.cuda.synchronize()
     assert nv.device_status() == 0
     ref, absref, out_bits = oracle.gemm(ac, asf, ga, wc, wsf, gw, residual=res_bits)
@@ -111,15 +112,17 @@ def test_deterministic(nv, ws):
 
 
 @pytest.mark.parametrize("M,N,K", [(1024, 7168, 5120), (1024, 5120, 17408), (1, 5120, 17408)])
-def test_full_size_sampled(nv, ws, M, N, K):
+@pytest.mark.parametrize("split", [False, True])
+def test_full_size_sampled(nv, ws, M, N, K, split):
     """Full projection sizes of the 27B-class model (QKV, down): quantized
-    operands compared in full, GEMM outputs on 2048 sampled elements."""
+    operands compared in full, GEMM outputs on 2048 sampled elements; with and
+    without the workspace that lets the GEMM split tiles over all SMs."""
     rng = np.random.default_rng(M + N)
     a = synthetic.normal(rng, (M, K))
     w = synthetic.normal(rng, (N, K), std=0.02)
     A, W = quantize_gpu(a, ws), quantize_gpu(w, ws)
     out = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
-    nv.nvfp4_gemm(A, W, out)
+    nv.nvfp4_gemm(A, W, out, workspace=nv.workspace(nv.gemm_workspace_bytes()) if split else None)
     ac, asf, ga = oracle_quant(a)
     wc, wsf, gw = oracle_quant(w)
     assert_same_quant(A, ac, asf, ga, "A")
@@ -133,3 +136,36 @@ def test_full_size_sampled(nv, ws, M, N, K):
     alpha = float(np.float32(np.float32(ga) * np.float32(gw)))
     got = f64(host(out))[m, n]
     check_close(got, alpha * dot, alpha * adot, f"{M}x{N}x{K} sampled")
+
+
+# Split schedule: the tiles' K ranges spread over all SMs, fp32 partials
+# combined through the workspace.  Deep-K shapes whose tiles leave most SMs
+# idle (so the split is taken), including a ragged M and a K with a partial
+# last stage (K = 8384: 32 full stages of 256 + 192).
+@pytest.mark.parametrize("M,N,K", [(777, 512, 8192), (300, 1024, 8192), (300, 768, 8384), (1, 5120, 8192)])
+def test_split_schedule(nv, ws, M, N, K):
+    got, ref, absref = run_case(nv, ws, M, N, K, seed=M + 7 * N + K, split=True)
+    check_close(got, ref, absref, f"{M}x{N}x{K} split")
+
+
+def test_split_residual_and_repeat(nv, ws):
+    """Residual add through the split schedule; two calls on one workspace
+    (its ready flags return to zero) give identical outputs, and these agree
+    with the unsplit schedule within the GEMM tolerance."""
+    rng = np.random.default_rng(21)
+    M, N, K = 300, 1024, 8192
+    A = quantize_gpu(synthetic.normal(rng, (M, K)), ws)
+    W = quantize_gpu(synthetic.normal(rng, (N, K), std=0.02), ws)
+    r = dev(synthetic.normal(rng, (M, N)))
+    gws = nv.workspace(nv.gemm_workspace_bytes())
+    o1 = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    o2, o3 = torch.empty_like(o1), torch.empty_like(o1)
+    nv.nvfp4_gemm(A, W, o1, residual=r, workspace=gws)
+    nv.nvfp4_gemm(A, W, o2, residual=r, workspace=gws)
+    nv.nvfp4_gemm(A, W, o3, residual=r)
+    torch.cuda.synchronize()
+    assert nv.device_status() == 0
+    assert torch.equal(o1, o2)
+    assert int(gws[:8192].count_nonzero()) == 0          # flags back to zero
+    d = (o1.double() - o3.double()).abs()
+    assert float(d.max()) <= 2 ** -7 * float(o3.double().abs().max()) + 1e-2

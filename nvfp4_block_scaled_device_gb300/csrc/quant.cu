@@ -1,9 +1,10 @@
 // Row kernels of the NVFP4 path: the device global scale (amax reduction,
 // optionally of the RMSNorm of the rows) and the bf16 -> NVFP4 quantizer
-// (optionally fused with that RMSNorm).  One warp per row (8 rows per
-// block, no block-wide barriers), 16-byte vector loads with 4 in flight per
-// lane, shuffle reductions; both kernels share one row routine so the
-// RMSNorm they compute is bit-identical.
+// (optionally fused with that RMSNorm).  Four warps per row (two rows per
+// 256-thread block, at least three blocks per SM), 16-byte vector loads, a
+// row share of up to 1536 columns per warp held in registers, shuffle
+// reductions; both kernels share one row routine so the RMSNorm they
+// compute is bit-identical.
 //
 // Sources: "PERFORMANCE -- verified hot-path audit and prioritized fixes"
 // P0 (scale = max(amax, 1e-8) / (6 * 448), computed on the device, handed on
@@ -17,8 +18,6 @@ namespace nvfp4 {
 
 namespace {
 
-constexpr int kRowsPerBlock = kRowThreads / 32;   // one warp per row
-constexpr int kUnroll = 4;                          // 16-byte loads in flight per lane
 
 __device__ __forceinline__ void unpack8(const uint4& p, float* f)
 {
@@ -68,118 +67,202 @@ __device__ __forceinline__ void norm8(float* f, float r, const uint4& wp)
     for (int i = 0; i < 8; i++) f[i] = bf16_round(__fmul_rn(__fmul_rn(f[i], r), w[i]));
 }
 
-// 1 / sqrt(mean(x^2) + eps) of one row, computed by one warp in a fixed
-// order.  The squares of bf16 values are exact in binary32; each lane sums
-// its squares as a float-float pair, the pairs are reduced by shuffles, and
-// lane 0 forms the mean in binary64 and rounds it once to binary32 -- the
-// binary64 mean-square of the definition, to far below half a binary32 ulp.
-// Every lane gets lane 0's result.
-__device__ __forceinline__ float warp_inv_rms(const uint4* __restrict__ xr, int64_t nvec, int64_t cols, float eps)
+// A row is shared by kWarpsPerRow warps: warp q of the row takes the
+// 256-column groups q, q + kWarpsPerRow, ... (group j = vectors 32j..32j+31,
+// lane l holding vector 32j + l), so a 16-element block sits in a lane pair
+// and a 64-element scale word in 8 lanes of one warp.  Up to kRegGroups
+// groups of a warp's share are held in registers (rows of up to
+// kWarpsPerRow * kRegGroups * 256 = 6144 columns are read once); longer rows
+// are read twice (sum of squares, then the row).
+constexpr int kWarpsPerRow = 4;
+constexpr int kRowsPerBlock = kRowThreads / 32 / kWarpsPerRow;   // 2
+constexpr int kRegGroups = 6;
+
+// Per-row scratch of a block: each warp's float-float sum of squares.
+struct RowShared {
+    float hi[kRowsPerBlock][kWarpsPerRow];
+    float lo[kRowsPerBlock][kWarpsPerRow];
+};
+
+// Float-float sum of squares of this lane's vectors in its warp's share of
+// the row, shuffle-reduced over the warp (fixed order).
+__device__ __forceinline__ FF warp_sumsq(const uint4* __restrict__ b, int ng)
 {
-    const int lane = threadIdx.x & 31;
     FF part{0.0f, 0.0f};
-    for (int64_t v0 = 0; v0 < nvec; v0 += 32 * kUnroll) {
-        uint4 b[kUnroll];
-#pragma unroll
-        for (int k = 0; k < kUnroll; k++) {
-            const int64_t v = v0 + 32 * k + lane;
-            b[k] = v < nvec ? xr[v] : make_uint4(0, 0, 0, 0);
-        }
-#pragma unroll
-        for (int k = 0; k < kUnroll; k++) part = ff_sumsq8(part, b[k]);
-    }
+    for (int k = 0; k < ng; k++) part = ff_sumsq8(part, b[k]);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
         FF other{__shfl_xor_sync(0xffffffffu, part.hi, o), __shfl_xor_sync(0xffffffffu, part.lo, o)};
         part = ff_add(part, other);
     }
-    float r = 0.0f;
-    if (lane == 0) {
-        const double sum = (double)part.hi + (double)part.lo;
-        const float ms = (float)(sum / (double)cols);
-        r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, eps)));
-    }
-    return __shfl_sync(0xffffffffu, r, 0);
+    return part;
 }
 
-// One row, one warp.  QUANT: quantize and store the row; otherwise
-// accumulate the amax of the (normalised) row into *amax.  The amax and the
-// quantize kernels both go through here, so their RMSNorm is bit-identical.
+// 1 / sqrt(mean(x^2) + eps) of the row from its warps' sums, combined in
+// warp order (lane 0 of every warp of the row computes the same value).  The
+// squares of bf16 values are exact in binary32 and the float-float sum S =
+// hi + lo carries far more precision than binary32.  The mean S / cols is
+// rounded once to binary32 without binary64 (slow here): q = hi / n, the
+// exact remainder hi - q n by a fused multiply-add, and the correction
+// (remainder + lo) / n added to q.  The result is the correctly rounded
+// quotient except within about 2^-24 of an ulp of a tie -- the same margin at
+// which the float-float sum itself may differ from the exact sum.
+__device__ __forceinline__ float row_inv_rms(const RowShared& sh, int rb, int64_t cols, float eps)
+{
+    FF t{sh.hi[rb][0], sh.lo[rb][0]};
+#pragma unroll
+    for (int q = 1; q < kWarpsPerRow; q++) t = ff_add(t, FF{sh.hi[rb][q], sh.lo[rb][q]});
+    const float n = (float)cols;                        // exact: cols < 2^24
+    const float q0 = __fdiv_rn(t.hi, n);
+    const float rem = __fmaf_rn(-q0, n, t.hi);          // exact
+    const float ms = __fadd_rn(q0, __fdiv_rn(__fadd_rn(rem, t.lo), n));
+    return __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, eps)));
+}
+
+// One 8-element vector v of a row, already in f (normalised when NORM):
+// QUANT: its half of a 16-element block quantized and stored (lanes 2j and
+// 2j+1 hold the two halves of a block); otherwise its amax folded in.
 template <bool NORM, bool QUANT>
-__device__ __forceinline__ void row_warp(const uint4* __restrict__ xr, int64_t row, int64_t nvec, int64_t cols,
-                                         const uint4* __restrict__ w, float eps, float g,
+__device__ __forceinline__ void vec_step(float* f, int64_t v, bool valid, int64_t row, int64_t cols, float g,
                                          uint8_t* __restrict__ codes, int64_t ld_codes, uint8_t* __restrict__ sf,
                                          int64_t kb_pad, __nv_bfloat16* __restrict__ y_out, float* amax)
 {
-    const int lane = threadIdx.x & 31;
-    const float r = NORM ? warp_inv_rms(xr, nvec, cols, eps) : 1.0f;
-    for (int64_t v0 = 0; v0 < nvec; v0 += 32 * kUnroll) {
-        uint4 b[kUnroll];
+    if (QUANT) {
+        if (NORM && y_out && valid) {
+            uint4 o;
+            o.x = pack_bf16x2(f[0], f[1]);
+            o.y = pack_bf16x2(f[2], f[3]);
+            o.z = pack_bf16x2(f[4], f[5]);
+            o.w = pack_bf16x2(f[6], f[7]);
+            reinterpret_cast<uint4*>(y_out + row * cols)[v] = o;
+        }
+        float a = 0.0f;
 #pragma unroll
-        for (int k = 0; k < kUnroll; k++) {
-            const int64_t v = v0 + 32 * k + lane;
-            b[k] = v < nvec ? xr[v] : make_uint4(0, 0, 0, 0);
+        for (int i = 0; i < 8; i++) a = fmaxf(a, fabsf(f[i]));
+        const float a16 = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
+        uint32_t sc;
+        const uint32_t cw = quant_half_block(f, g, a16, &sc);
+        const uint32_t s1 = __shfl_down_sync(0xffffffffu, sc, 2);
+        const uint32_t s2 = __shfl_down_sync(0xffffffffu, sc, 4);
+        const uint32_t s3 = __shfl_down_sync(0xffffffffu, sc, 6);
+        if (valid) {
+            *reinterpret_cast<uint32_t*>(codes + row * ld_codes + v * 4) = cw;
+            if ((v & 7) == 0)
+                *reinterpret_cast<uint32_t*>(sf + sf_offset(row, v / 2, kb_pad)) =
+                    sc | (s1 << 8) | (s2 << 16) | (s3 << 24);
+        }
+    } else if (valid) {
+#pragma unroll
+        for (int i = 0; i < 8; i++) *amax = fmaxf(*amax, fabsf(f[i]));
+    }
+}
+
+// This warp's share of one row (row < rows; rb = the row's slot in the
+// block, q = the warp's index within the row).  QUANT: quantize and store
+// the share; otherwise accumulate its amax (of the normalised row) into
+// *amax.  The amax and the quantize kernels both go through here, so the
+// RMSNorm they compute is bit-identical.  The block's barrier is executed
+// by every warp (NORM only), whatever its row.
+template <bool NORM, bool QUANT>
+__device__ __forceinline__ void row_share(const uint4* __restrict__ xr, int64_t row, bool row_valid, int rb, int q,
+                                          int64_t nvec, int64_t cols, const uint4* __restrict__ w, float eps,
+                                          float g, uint8_t* __restrict__ codes, int64_t ld_codes,
+                                          uint8_t* __restrict__ sf, int64_t kb_pad, __nv_bfloat16* __restrict__ y_out,
+                                          float* amax, RowShared& sh)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t ngroups = (nvec + 31) / 32;
+    const int ng = row_valid ? (int)((ngroups - q + kWarpsPerRow - 1) / kWarpsPerRow) : 0;   // this warp's groups
+    if (ng <= kRegGroups) {
+        uint4 b[kRegGroups];
+#pragma unroll
+        for (int k = 0; k < kRegGroups; k++) {
+            const int64_t v = (int64_t)(q + k * kWarpsPerRow) * 32 + lane;
+            b[k] = (k < ng && v < nvec) ? xr[v] : make_uint4(0, 0, 0, 0);
+        }
+        float r = 1.0f;
+        if (NORM) {
+            const FF part = warp_sumsq(b, kRegGroups);   // zero padding adds exact zeros
+            if (lane == 0) {
+                sh.hi[rb][q] = part.hi;
+                sh.lo[rb][q] = part.lo;
+            }
+            __syncthreads();
+            // one lane per warp (binary64 is slow on this GPU), then broadcast
+            if (row_valid && lane == 0) r = row_inv_rms(sh, rb, cols, eps);
+            r = __shfl_sync(0xffffffffu, r, 0);
+            __syncthreads();                            // sh is reused by the block's next rows
         }
 #pragma unroll
-        for (int k = 0; k < kUnroll; k++) {
-            const int64_t v = v0 + 32 * k + lane;
-            const bool valid = v < nvec;            // uniform over each group of 8 lanes
+        for (int k = 0; k < kRegGroups; k++) {
+            if (k >= ng) break;                         // uniform over the warp
+            const int64_t v = (int64_t)(q + k * kWarpsPerRow) * 32 + lane;
+            const bool valid = v < nvec;                // uniform over each group of 8 lanes
             float f[8];
             unpack8(b[k], f);
             if (NORM && valid) norm8(f, r, w[v]);
-            if (QUANT) {
-                if (NORM && y_out && valid) {
-                    uint4 o;
-                    o.x = pack_bf16x2(f[0], f[1]);
-                    o.y = pack_bf16x2(f[2], f[3]);
-                    o.z = pack_bf16x2(f[4], f[5]);
-                    o.w = pack_bf16x2(f[6], f[7]);
-                    reinterpret_cast<uint4*>(y_out + row * cols)[v] = o;
-                }
-                float a = 0.0f;
-#pragma unroll
-                for (int i = 0; i < 8; i++) a = fmaxf(a, fabsf(f[i]));
-                const float a16 = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
-                uint32_t sc;
-                const uint32_t cw = quant_half_block(f, g, a16, &sc);
-                const uint32_t s1 = __shfl_down_sync(0xffffffffu, sc, 2);
-                const uint32_t s2 = __shfl_down_sync(0xffffffffu, sc, 4);
-                const uint32_t s3 = __shfl_down_sync(0xffffffffu, sc, 6);
-                if (valid) {
-                    *reinterpret_cast<uint32_t*>(codes + row * ld_codes + v * 4) = cw;
-                    if ((v & 7) == 0)
-                        *reinterpret_cast<uint32_t*>(sf + sf_offset(row, v / 2, kb_pad)) =
-                            sc | (s1 << 8) | (s2 << 16) | (s3 << 24);
-                }
-            } else if (valid) {
-#pragma unroll
-                for (int i = 0; i < 8; i++) *amax = fmaxf(*amax, fabsf(f[i]));
-            }
+            vec_step<NORM, QUANT>(f, v, valid, row, cols, g, codes, ld_codes, sf, kb_pad, y_out, amax);
         }
+        return;
+    }
+    // long rows: sum of squares over the share, then the share again
+    float r = 1.0f;
+    if (NORM) {
+        FF part{0.0f, 0.0f};
+        for (int k = 0; k < ng; k++) {
+            const int64_t v = (int64_t)(q + k * kWarpsPerRow) * 32 + lane;
+            part = ff_sumsq8(part, v < nvec ? xr[v] : make_uint4(0, 0, 0, 0));
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            FF other{__shfl_xor_sync(0xffffffffu, part.hi, o), __shfl_xor_sync(0xffffffffu, part.lo, o)};
+            part = ff_add(part, other);
+        }
+        if (lane == 0) {
+            sh.hi[rb][q] = part.hi;
+            sh.lo[rb][q] = part.lo;
+        }
+        __syncthreads();
+        if (lane == 0) r = row_inv_rms(sh, rb, cols, eps);
+        r = __shfl_sync(0xffffffffu, r, 0);
+        __syncthreads();
+    }
+    for (int k = 0; k < ng; k++) {
+        const int64_t v = (int64_t)(q + k * kWarpsPerRow) * 32 + lane;
+        const bool valid = v < nvec;
+        float f[8];
+        unpack8(v < nvec ? xr[v] : make_uint4(0, 0, 0, 0), f);
+        if (NORM && valid) norm8(f, r, w[v]);
+        vec_step<NORM, QUANT>(f, v, valid, row, cols, g, codes, ld_codes, sf, kb_pad, y_out, amax);
     }
 }
 
 template <bool NORM>
-__global__ void __launch_bounds__(kRowThreads) amax_scale_kernel(const __nv_bfloat16* __restrict__ x, int64_t rows,
+__global__ void __launch_bounds__(kRowThreads, 3) amax_scale_kernel(const __nv_bfloat16* __restrict__ x, int64_t rows,
                                                                  int64_t cols, int64_t ldx,
                                                                  const __nv_bfloat16* __restrict__ norm_w,
                                                                  float eps, float* __restrict__ g_out,
                                                                  uint32_t* __restrict__ ws)
 {
+    __shared__ RowShared sh;
     const int64_t nvec = cols / 8;
+    const int wib = threadIdx.x >> 5, rb = wib / kWarpsPerRow, q = wib % kWarpsPerRow;
     float amax = 0.0f;
-    for (int64_t row = (int64_t)blockIdx.x * kRowsPerBlock + (threadIdx.x >> 5); row < rows;
-         row += (int64_t)gridDim.x * kRowsPerBlock)
-        row_warp<NORM, false>(reinterpret_cast<const uint4*>(x + row * ldx), row, nvec, cols,
-                              reinterpret_cast<const uint4*>(norm_w), eps, 0.0f, nullptr, 0, nullptr, 0, nullptr,
-                              &amax);
+    // every warp of the block runs the same number of iterations (barriers)
+    for (int64_t r0 = (int64_t)blockIdx.x * kRowsPerBlock; r0 < rows; r0 += (int64_t)gridDim.x * kRowsPerBlock) {
+        const int64_t row = r0 + rb;
+        const bool ok = row < rows;
+        row_share<NORM, false>(reinterpret_cast<const uint4*>(x + (ok ? row : 0) * ldx), row, ok, rb, q, nvec, cols,
+                               reinterpret_cast<const uint4*>(norm_w), eps, 0.0f, nullptr, 0, nullptr, 0, nullptr,
+                               &amax, sh);
+    }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    __shared__ float wmax[kRowsPerBlock];
-    if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = amax;
+    __shared__ float wmax[kRowThreads / 32];
+    if ((threadIdx.x & 31) == 0) wmax[wib] = amax;
     __syncthreads();
     if (threadIdx.x == 0) {
-        for (int w = 1; w < kRowsPerBlock; w++) amax = fmaxf(amax, wmax[w]);
+        for (int w = 1; w < kRowThreads / 32; w++) amax = fmaxf(amax, wmax[w]);
         // non-negative binary32 values order like their bit patterns
         atomicMax(&ws[0], __float_as_uint(amax));
         __threadfence();
@@ -194,7 +277,7 @@ __global__ void __launch_bounds__(kRowThreads) amax_scale_kernel(const __nv_bflo
 }
 
 template <bool NORM>
-__global__ void __launch_bounds__(kRowThreads) quantize_kernel(const __nv_bfloat16* __restrict__ x, int64_t rows,
+__global__ void __launch_bounds__(kRowThreads, 3) quantize_kernel(const __nv_bfloat16* __restrict__ x, int64_t rows,
                                                                int64_t cols, int64_t ldx,
                                                                const __nv_bfloat16* __restrict__ norm_w, float eps,
                                                                const float* __restrict__ g_ptr,
@@ -202,22 +285,25 @@ __global__ void __launch_bounds__(kRowThreads) quantize_kernel(const __nv_bfloat
                                                                uint8_t* __restrict__ sf,
                                                                __nv_bfloat16* __restrict__ y_out)
 {
+    __shared__ RowShared sh;
     const float g = *g_ptr;
     const int64_t nvec = cols / 8;          // a multiple of 8: cols % 64 == 0
     const int64_t kb_pad = cols / 16;       // already a multiple of 4
     const int64_t pad_rows = (rows + 127) / 128 * 128;
     const int lane = threadIdx.x & 31;
-    for (int64_t row = (int64_t)blockIdx.x * kRowsPerBlock + (threadIdx.x >> 5); row < pad_rows;
-         row += (int64_t)gridDim.x * kRowsPerBlock) {
-        if (row >= rows) {
+    const int wib = threadIdx.x >> 5, rb = wib / kWarpsPerRow, q = wib % kWarpsPerRow;
+    // every warp of the block runs the same number of iterations (barriers)
+    for (int64_t r0 = (int64_t)blockIdx.x * kRowsPerBlock; r0 < pad_rows; r0 += (int64_t)gridDim.x * kRowsPerBlock) {
+        const int64_t row = r0 + rb;
+        if (row >= rows && row < pad_rows) {
             // padding rows of the scale layout are zero
-            for (int64_t c4 = lane; c4 < kb_pad / 4; c4 += 32)
+            for (int64_t c4 = (int64_t)q * 32 + lane; c4 < kb_pad / 4; c4 += 32 * kWarpsPerRow)
                 *reinterpret_cast<uint32_t*>(sf + sf_offset(row, c4 * 4, kb_pad)) = 0u;
-            continue;
         }
-        row_warp<NORM, true>(reinterpret_cast<const uint4*>(x + row * ldx), row, nvec, cols,
-                             reinterpret_cast<const uint4*>(norm_w), eps, g, codes, ld_codes, sf, kb_pad, y_out,
-                             nullptr);
+        const bool ok = row < rows;
+        row_share<NORM, true>(reinterpret_cast<const uint4*>(x + (ok ? row : 0) * ldx), row, ok, rb, q, nvec, cols,
+                              reinterpret_cast<const uint4*>(norm_w), eps, g, codes, ld_codes, sf, kb_pad, y_out,
+                              nullptr, sh);
     }
 }
 

@@ -164,6 +164,26 @@ int nvfp4_quantize(const void* x, int64_t rows, int64_t cols, int64_t ldx,
                    nvfp4_stream_t stream);
 
 /*
+ * nvfp4_scale_quantize -- nvfp4_amax_scale then nvfp4_quantize with the
+ * scale just computed, as ONE kernel launch: *g_out, codes and sf are bit for
+ * bit those of the two calls.  The kernel is a cooperative launch with one
+ * grid-wide barrier between the amax and the quantization (every block is
+ * resident; when the grid covers all rows at once each row is read once).
+ * Sources: as nvfp4_amax_scale and nvfp4_quantize.
+ *   x, ldx, norm_w, eps  as nvfp4_amax_scale.
+ *   g_out    fp32[1], written with the global scale.
+ *   codes, ld_codes, sf  as nvfp4_quantize.
+ *   workspace as nvfp4_amax_scale (>= nvfp4_amax_workspace_bytes(), zero-filled
+ *            once; calls leave it zeroed).  After a call that reported a
+ *            timeout through nvfp4_device_status it must be zero-filled again.
+ * Requires rows >= 1, cols % 64 == 0.
+ */
+int nvfp4_scale_quantize(const void* x, int64_t rows, int64_t cols, int64_t ldx,
+                         const void* norm_w, float eps, float* g_out,
+                         uint8_t* codes, int64_t ld_codes, uint8_t* sf,
+                         void* workspace, size_t workspace_bytes, nvfp4_stream_t stream);
+
+/*
  * nvfp4_gemm -- block-scaled GEMM on the tensor cores (tcgen05
  * kind::mxf4nvf4, fp32 accumulation in tensor memory):
  *   out[m][n] = bf16( alpha * sum_k A[m,k] W[n,k] ),  alpha = fp32(gA * gW),

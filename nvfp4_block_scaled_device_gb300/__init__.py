@@ -50,6 +50,10 @@ _SIGS = {
     "nvfp4_quantize": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
                                       ctypes.c_void_p, ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p,
                                       ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
+    "nvfp4_scale_quantize": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                            ctypes.c_void_p, ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p,
+                                            ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t,
+                                            ctypes.c_void_p]),
     "nvfp4_gemm": (ctypes.c_int, [ctypes.POINTER(_TensorC), ctypes.POINTER(_TensorC), ctypes.c_void_p,
                                   ctypes.c_int64, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p,
                                   ctypes.c_size_t, ctypes.c_void_p]),
@@ -193,6 +197,14 @@ def nvfp4_quantize(x: torch.Tensor, g: torch.Tensor, out: NVFP4Tensor, norm_w=No
     _check(lib().nvfp4_quantize(_ptr(x), rows, cols, ldx, _ptr(norm_w), eps, _ptr(g), _ptr(out.codes),
                                 out.codes.stride(0), _ptr(out.sf), _ptr(y_out), _stream(stream)),
            "nvfp4_quantize")
+
+
+def nvfp4_scale_quantize(x: torch.Tensor, out: NVFP4Tensor, ws: torch.Tensor, norm_w=None, eps=1e-6, stream=None):
+    """Global scale into out.g and quantization into out, in one launch."""
+    rows, cols, ldx = _bf16_2d(x, "x")
+    _check(lib().nvfp4_scale_quantize(_ptr(x), rows, cols, ldx, _ptr(norm_w), eps, _ptr(out.g), _ptr(out.codes),
+                                      out.codes.stride(0), _ptr(out.sf), _ptr(ws), ws.numel() * ws.element_size(),
+                                      _stream(stream)), "nvfp4_scale_quantize")
 
 
 def quantize_new(x: torch.Tensor, ws: torch.Tensor, norm_w=None, eps=1e-6, stream=None) -> NVFP4Tensor:

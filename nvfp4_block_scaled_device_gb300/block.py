@@ -28,12 +28,11 @@ from __future__ import annotations
 import torch
 
 from . import (NVFP4_INTER_DYNAMIC, NVFP4_INTER_STATIC, NVFP4Tensor, gemm_workspace_bytes, mlp_workspace_bytes,
-               nvfp4_amax_scale,
-               nvfp4_gemm, nvfp4_gemm_swiglu, nvfp4_mlp, nvfp4_quantize, swiglu_workspace_bytes, workspace)
+               nvfp4_gemm, nvfp4_gemm_swiglu, nvfp4_mlp, nvfp4_scale_quantize, swiglu_workspace_bytes, workspace)
 
 
 class PrefillBlock:
-    LAUNCHES_PER_FORWARD = 10  # 2 norm+quant, 1 QKV, 2 stand-in quant, 1 O, 4 MLP (static scale)
+    LAUNCHES_PER_FORWARD = 7  # norm+scale+quant, QKV, stand-in scale+quant, O, 3 MLP (static scale)
 
     def __init__(self, T: int, weights: dict, attn_norm: torch.Tensor, mlp_norm: torch.Tensor, eps=1e-6):
         """weights: NVFP4Tensor values under 'qkv' [Nqkv x H], 'o' [H x H],
@@ -63,14 +62,12 @@ class PrefillBlock:
 
     def attention_part(self, x: torch.Tensor, stream=None, ev=None):
         rec = (lambda k: ev[k].record(stream)) if ev is not None else (lambda k: None)
-        nvfp4_amax_scale(x, self.h.g, self.ws_amax, self.attn_norm, self.eps, stream)
-        nvfp4_quantize(x, self.h.g, self.h, self.attn_norm, self.eps, None, stream)
+        nvfp4_scale_quantize(x, self.h, self.ws_amax, self.attn_norm, self.eps, stream)
         rec("qkv0")
         nvfp4_gemm(self.h, self.w["qkv"], self.qkv, None, stream, self.ws_gemm)
         rec("qkv1")
         q = self.qkv[:, :self.H]
-        nvfp4_amax_scale(q, self.a.g, self.ws_amax, None, self.eps, stream)
-        nvfp4_quantize(q, self.a.g, self.a, None, self.eps, None, stream)
+        nvfp4_scale_quantize(q, self.a, self.ws_amax, None, self.eps, stream)
         rec("o0")
         nvfp4_gemm(self.a, self.w["o"], self.x1, x, stream, self.ws_gemm)
         rec("o1")
@@ -89,13 +86,12 @@ class PrefillBlock:
                   self.g_inter, out, self.ws_mlp, True, self.eps, stream)
 
     def forward_timed(self, x: torch.Tensor, out: torch.Tensor, ev: dict, stream=None):
-        """forward() with the MLP launched through its parts (the same four
+        """forward() with the MLP launched through its parts (the same three
         kernels nvfp4_mlp launches) and CUDA events around each GEMM."""
         rec = lambda k: ev[k].record(stream)
         self.attention_part(x, stream, ev)
         rec("mlp0")
-        nvfp4_amax_scale(self.x1, self.hm.g, self.ws_amax, self.mlp_norm, self.eps, stream)
-        nvfp4_quantize(self.x1, self.hm.g, self.hm, self.mlp_norm, self.eps, None, stream)
+        nvfp4_scale_quantize(self.x1, self.hm, self.ws_amax, self.mlp_norm, self.eps, stream)
         rec("gu0")
         nvfp4_gemm_swiglu(self.hm, self.w["gate"], self.w["up"], NVFP4_INTER_STATIC, self.g_inter, self.s,
                           self.ws_swiglu, None, stream)

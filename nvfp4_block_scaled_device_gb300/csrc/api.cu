@@ -361,6 +361,26 @@ int nvfp4_quantize(const void* x, int64_t rows, int64_t cols, int64_t ldx, const
     return NVFP4_OK;
 }
 
+int nvfp4_scale_quantize(const void* x, int64_t rows, int64_t cols, int64_t ldx, const void* norm_w, float eps,
+                         float* g_out, uint8_t* codes, int64_t ld_codes, uint8_t* sf, void* workspace,
+                         size_t workspace_bytes, nvfp4_stream_t stream)
+{
+    NVFP4_TRY(check_bf16_matrix(x, rows, cols, ldx));
+    if (cols % 64 != 0 || !g_out || !codes || !sf || ld_codes < cols / 2) return NVFP4_ERR_INVALID_ARG;
+    if (!aligned(codes, 16) || ld_codes % 16 != 0 || !aligned(sf, 128) || !aligned(g_out, 4))
+        return NVFP4_ERR_MISALIGNED;
+    if (norm_w && !aligned(norm_w, 16)) return NVFP4_ERR_MISALIGNED;
+    if (!workspace || workspace_bytes < kAmaxWorkspaceBytes) return NVFP4_ERR_WORKSPACE;
+    if (!aligned(workspace, 256)) return NVFP4_ERR_MISALIGNED;
+    DeviceInfo* d = nullptr;
+    NVFP4_TRY(device_info(&d));
+    NVFP4_CUDA(launch_scale_quantize(static_cast<const __nv_bfloat16*>(x), rows, cols, ldx,
+                                     static_cast<const __nv_bfloat16*>(norm_w), eps, g_out, codes, ld_codes, sf,
+                                     static_cast<uint32_t*>(workspace), d->status, d->num_sms,
+                                     (cudaStream_t)stream));
+    return NVFP4_OK;
+}
+
 int nvfp4_gemm(const nvfp4_tensor_t* A, const nvfp4_tensor_t* W, void* out, int64_t ldo, const void* residual,
                int64_t ldr, void* workspace, size_t workspace_bytes, nvfp4_stream_t stream)
 {
@@ -454,7 +474,7 @@ int nvfp4_mlp(const void* x, int64_t T, int64_t H, int64_t ldx, const void* norm
     cudaStream_t st = (cudaStream_t)stream;
 
     uint8_t* ws = static_cast<uint8_t*>(workspace);
-    uint32_t* amax_ws = reinterpret_cast<uint32_t*>(ws);          // words [0,2)
+    uint32_t* amax_ws = reinterpret_cast<uint32_t*>(ws);          // words [0,3)
     float* g_h = reinterpret_cast<float*>(ws + 64);
     const SplitScratch split = split_scratch(d, ws + 256, ws + base, workspace_bytes - base);
     size_t off = 256 + kSplitFlagBytes;
@@ -471,8 +491,8 @@ int nvfp4_mlp(const void* x, int64_t T, int64_t H, int64_t ldx, const void* norm
     const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
     const __nv_bfloat16* nw = static_cast<const __nv_bfloat16*>(norm_w);
     // 1-2: RMSNorm prologue -> device scale -> FP4 input
-    NVFP4_CUDA(launch_amax_scale(xb, T, H, ldx, nw, eps, g_h, amax_ws, d->num_sms, st));
-    NVFP4_CUDA(launch_quantize(xb, T, H, ldx, nw, eps, g_h, h_codes, H / 2, h_sf, nullptr, d->num_sms, st));
+    NVFP4_CUDA(launch_scale_quantize(xb, T, H, ldx, nw, eps, g_h, h_codes, H / 2, h_sf, amax_ws, d->status,
+                                     d->num_sms, st));
     // 3: fused gate/up GEMM + SwiGLU + FP4 requant
     const nvfp4_tensor_t h = {h_codes, h_sf, g_h, T, H, H / 2};
     // the gate/up kernel and the down kernel run one after the other on the

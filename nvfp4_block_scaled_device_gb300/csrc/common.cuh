@@ -749,9 +749,10 @@ __device__ __forceinline__ int64_t sf_offset(int64_t r, int64_t c, int64_t kb_pa
 __device__ __forceinline__ float div_by_recip(float a, float b, float y)
 {
     const float q0 = __fmul_rn(a, y);
-    const float r = __fmaf_rn(-q0, b, a);
-    // b > 0: the quotient has a's sign; this also keeps -0 / b = -0
-    return copysignf(__fmaf_rn(r, y, q0), a);
+    // t = q0*b - a, the negated remainder, so that the final sum keeps the
+    // sign of a zero quotient: a = -0 gives q0 = -0, t = +0, -t*y + q0 = -0
+    const float t = __fmaf_rn(q0, b, -a);
+    return __fmaf_rn(-t, y, q0);
 }
 
 // Quantize one 16-element block held as two halves of 8 in lanes l, l^1:
@@ -762,8 +763,11 @@ __device__ __forceinline__ float div_by_recip(float a, float b, float y)
 // den = E4M3val(s)*g, code_i = E2M1(v_i/den).
 __device__ __forceinline__ uint32_t quant_half_block(const float* v, float g, float amax16, uint32_t* sc_out)
 {
+    // d, its reciprocal: the same for every block of a tensor (hoisted out of
+    // the callers' loops); amax16 / d by the quotient refinement above
+    // (a quotient below 2^-126 would round to a zero scale either way)
     const float d = __fmul_rn(6.0f, g);
-    const float s_raw = __fdiv_rn(amax16, d);
+    const float s_raw = div_by_recip(amax16, d, __frcp_rn(d));
     const uint32_t sc = cvt_e4m3(s_raw);
     *sc_out = sc;
     if (sc == 0) return 0u;

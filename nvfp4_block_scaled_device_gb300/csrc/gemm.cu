@@ -91,7 +91,7 @@ __device__ unsigned long long g_trace[1280];
 // accumulator ready, [c][2] first segment's partial stored or tile
 // finished, [c][3] last segment finished.
 __device__ unsigned long long g_trace_cta[256][4];
-__device__ unsigned long long g_trace_fix[16];   // CTA 0, first epilogue warp: each contributor's flag seen
+__device__ unsigned long long g_trace_fix[16];   // CTA 0, first epilogue warp: [c] contributor c's flag seen, [0] partials added
 #define TRACE_CTA(k) \
     do { if (blockIdx.x < 256) g_trace_cta[blockIdx.x][k] = globaltimer(); } while (0)
 #else
@@ -544,6 +544,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     }
                 }
                 __syncwarp();
+#ifdef NVFP4_TRACE
+                if (blockIdx.x == 0 && warp == kEpiWarp0 && lane == 0) g_trace_fix[0] = globaltimer();
+#endif
                 if (lane == 0)
                     for (int64_t c = (int64_t)blockIdx.x + 1; c < c_end; c++) args.sk_flags[c * kSplitFlagsPerCta + we] = 0;
                 if (warp == kEpiWarp0 && lane == 0) TRACE(1216, ecount - 1);

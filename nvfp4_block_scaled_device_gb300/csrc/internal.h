@@ -20,8 +20,10 @@ constexpr int kRowThreads = 256;
 // several issuing lanes.
 constexpr int kCodeBoxRows = 64;
 
-// Workspace words used by the amax reduction: [0] amax bits, [1] ticket.
-constexpr size_t kAmaxWorkspaceBytes = 8;
+// Workspace words used by the amax reduction: [0] amax bits, [1] ticket
+// (arrivals at the grid barrier of the fused scale + quantize kernels),
+// [2] departures from that barrier.
+constexpr size_t kAmaxWorkspaceBytes = 16;
 
 cudaError_t launch_amax_scale(const __nv_bfloat16* x, int64_t rows, int64_t cols, int64_t ldx,
                               const __nv_bfloat16* norm_w, float eps, float* g_out, uint32_t* ws,
@@ -34,6 +36,14 @@ cudaError_t launch_quantize(const __nv_bfloat16* x, int64_t rows, int64_t cols, 
 
 // g_out = max(amax(ws), 1e-8) / 2688, and the amax word is reset to zero.
 cudaError_t launch_finalize_scale(uint32_t* ws, float* g_out, cudaStream_t stream);
+
+// launch_amax_scale followed by launch_quantize in one cooperative launch
+// (bit-identical results); sf padding rows are zero-filled.  A barrier wait
+// that gives up records a timeout in *status.
+cudaError_t launch_scale_quantize(const __nv_bfloat16* x, int64_t rows, int64_t cols, int64_t ldx,
+                                  const __nv_bfloat16* norm_w, float eps, float* g_out, uint8_t* codes,
+                                  int64_t ld_codes, uint8_t* sf, uint32_t* ws, int* status, int num_sms,
+                                  cudaStream_t stream);
 
 enum EpilogueKind : int {
     kEpiBf16 = 0,        // out = bf16(alpha * acc) [+ residual]

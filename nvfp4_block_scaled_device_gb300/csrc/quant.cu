@@ -313,6 +313,210 @@ __global__ void finalize_scale_kernel(uint32_t* ws, float* g_out)
     g_out[0] = __fdiv_rn(fmaxf(a, 1e-8f), 2688.0f);
 }
 
+// ---------------------------------------------- scale + quantize, one launch
+// The global scale needs the amax of the whole matrix before any block can
+// quantize, so the fused kernels run as cooperative launches (every block
+// resident) with one grid-wide barrier between the two phases.  Workspace
+// words: [0] amax bits (atomicMax), [1] arrivals, [2] departures; the last
+// block to depart returns all three to zero.
+
+// Block-wide amax of the per-thread values, merged into ws[0]; then the grid
+// barrier; returns the global scale to every thread of the block, or -1 if
+// the barrier wait gave up (status recorded).  Block 0 writes *g_out.
+__device__ float grid_global_scale(float amax, uint32_t* ws, float* g_out, int* status, int site)
+{
+    __shared__ float wmax[kRowThreads / 32];
+    __shared__ float s_g;
+    const int wib = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    if ((threadIdx.x & 31) == 0) wmax[wib] = amax;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        for (int w = 1; w < kRowThreads / 32; w++) amax = fmaxf(amax, wmax[w]);
+        // non-negative binary32 values order like their bit patterns
+        atomicMax(&ws[0], __float_as_uint(amax));
+        __threadfence();
+        atomicAdd(&ws[1], 1u);
+        const uint64_t t0 = clock64();
+        float g = -1.0f;
+        for (;;) {
+            uint32_t arrived;
+            asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(arrived) : "l"(ws + 1) : "memory");
+            if (arrived >= gridDim.x) {
+                uint32_t bits;
+                asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(bits) : "l"(ws) : "memory");
+                g = __fdiv_rn(fmaxf(__uint_as_float(bits), 1e-8f), 2688.0f);
+                break;
+            }
+            if ((uint64_t)(clock64() - t0) > kWaitLimitCycles) {
+                if (status) atomicCAS(status, 0, kErrTimeout * 100 + site);
+                break;
+            }
+            __nanosleep(64);
+        }
+        if (g >= 0.0f) {
+            if (blockIdx.x == 0) g_out[0] = g;
+            // every block has read the amax before it departs: the last one
+            // to depart clears the words for the next call
+            __threadfence();
+            if (atomicAdd(&ws[2], 1u) == gridDim.x - 1) {
+                atomicExch(&ws[0], 0u);
+                atomicExch(&ws[1], 0u);
+                atomicExch(&ws[2], 0u);
+            }
+        }
+        s_g = g;
+    }
+    __syncthreads();
+    return s_g;
+}
+
+// Scale rows [rows, pad128(rows)) of the swizzled layout must be zero.  The
+// last 128-row tile of the layout is one contiguous run of bytes: before the
+// grid barrier the whole grid clears it with 16-byte stores, and the
+// quantization after the barrier writes the tile's real rows over it.
+__device__ __forceinline__ void zero_last_scale_tile(uint8_t* __restrict__ sf, int64_t rows, int64_t kb_pad)
+{
+    if (rows % 128 == 0) return;
+    uint4* t = reinterpret_cast<uint4*>(sf + (rows / 128) * (kb_pad / 4) * 512);
+    const int64_t n = kb_pad * 8;                        // (kb_pad / 4) tiles of 32 vectors
+    for (int64_t i = (int64_t)blockIdx.x * kRowThreads + threadIdx.x; i < n; i += (int64_t)gridDim.x * kRowThreads)
+        t[i] = make_uint4(0, 0, 0, 0);
+}
+
+// Resident variant: one block per row pair (the grid covers every row at
+// once) and each warp's share of its row (at most kResGroups 256-column
+// groups) stays in registers across the barrier: the row is read once, its
+// RMSNorm computed once and held as bf16 for the quantizer.
+constexpr int kResGroups = 5;
+constexpr int kResMaxCols = kWarpsPerRow * kResGroups * 256;   // 5120
+
+template <bool NORM>
+__global__ void __launch_bounds__(kRowThreads, 4)
+    scale_quantize_resident_kernel(const __nv_bfloat16* __restrict__ x, int64_t rows, int64_t cols, int64_t ldx,
+                                   const __nv_bfloat16* __restrict__ norm_w, float eps, float* __restrict__ g_out,
+                                   uint8_t* __restrict__ codes, int64_t ld_codes, uint8_t* __restrict__ sf,
+                                   uint32_t* __restrict__ ws, int* status)
+{
+    __shared__ RowShared sh;
+    const int64_t nvec = cols / 8;
+    const int64_t kb_pad = cols / 16;
+    const int lane = threadIdx.x & 31;
+    const int wib = threadIdx.x >> 5, rb = wib / kWarpsPerRow, q = wib % kWarpsPerRow;
+    const int64_t row = (int64_t)blockIdx.x * kRowsPerBlock + rb;
+    const bool ok = row < rows;
+    const uint4* xr = reinterpret_cast<const uint4*>(x + (ok ? row : 0) * ldx);
+    const uint4* w = reinterpret_cast<const uint4*>(norm_w);
+    const int64_t ngroups = (nvec + 31) / 32;
+    const int ng = ok ? (int)((ngroups - q + kWarpsPerRow - 1) / kWarpsPerRow) : 0;
+    zero_last_scale_tile(sf, rows, kb_pad);
+
+    uint4 b[kResGroups];
+#pragma unroll
+    for (int k = 0; k < kResGroups; k++) {
+        const int64_t v = (int64_t)(q + k * kWarpsPerRow) * 32 + lane;
+        b[k] = (k < ng && v < nvec) ? xr[v] : make_uint4(0, 0, 0, 0);
+    }
+    float r = 1.0f;
+    if (NORM) {
+        const FF part = warp_sumsq(b, kResGroups);     // zero padding adds exact zeros
+        if (lane == 0) {
+            sh.hi[rb][q] = part.hi;
+            sh.lo[rb][q] = part.lo;
+        }
+        __syncthreads();
+        if (ok && lane == 0) r = row_inv_rms(sh, rb, cols, eps);
+        r = __shfl_sync(0xffffffffu, r, 0);
+    }
+    // phase 1: the row (normalised when NORM, kept as bf16) and its amax
+    float amax = 0.0f;
+#pragma unroll
+    for (int k = 0; k < kResGroups; k++) {
+        if (k >= ng) break;                             // uniform over the warp
+        const int64_t v = (int64_t)(q + k * kWarpsPerRow) * 32 + lane;
+        if (v >= nvec) break;                           // uniform over each group of 8 lanes
+        float f[8];
+        unpack8(b[k], f);
+        if (NORM) {
+            norm8(f, r, w[v]);
+            b[k] = make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
+                              pack_bf16x2(f[6], f[7]));
+        }
+#pragma unroll
+        for (int i = 0; i < 8; i++) amax = fmaxf(amax, fabsf(f[i]));
+    }
+    const float g = grid_global_scale(amax, ws, g_out, status, 7);
+    if (g < 0.0f) return;
+    // phase 2: quantize the held row
+#pragma unroll
+    for (int k = 0; k < kResGroups; k++) {
+        if (k >= ng) break;
+        const int64_t v = (int64_t)(q + k * kWarpsPerRow) * 32 + lane;
+        const bool valid = v < nvec;
+        float f[8];
+        unpack8(b[k], f);
+        vec_step<false, true>(f, v, valid, row, cols, g, codes, ld_codes, sf, kb_pad, nullptr, nullptr);
+    }
+}
+
+// General variant: blocks loop over the rows in both phases (the rows are
+// read twice, as by the two separate kernels).
+template <bool NORM>
+__global__ void __launch_bounds__(kRowThreads, 3)
+    scale_quantize_kernel(const __nv_bfloat16* __restrict__ x, int64_t rows, int64_t cols, int64_t ldx,
+                          const __nv_bfloat16* __restrict__ norm_w, float eps, float* __restrict__ g_out,
+                          uint8_t* __restrict__ codes, int64_t ld_codes, uint8_t* __restrict__ sf,
+                          uint32_t* __restrict__ ws, int* status)
+{
+    __shared__ RowShared sh;
+    const int64_t nvec = cols / 8;
+    const int64_t kb_pad = cols / 16;
+    const int wib = threadIdx.x >> 5, rb = wib / kWarpsPerRow, q = wib % kWarpsPerRow;
+    zero_last_scale_tile(sf, rows, kb_pad);
+    float amax = 0.0f;
+    for (int64_t r0 = (int64_t)blockIdx.x * kRowsPerBlock; r0 < rows; r0 += (int64_t)gridDim.x * kRowsPerBlock) {
+        const int64_t row = r0 + rb;
+        const bool ok = row < rows;
+        row_share<NORM, false>(reinterpret_cast<const uint4*>(x + (ok ? row : 0) * ldx), row, ok, rb, q, nvec, cols,
+                               reinterpret_cast<const uint4*>(norm_w), eps, 0.0f, nullptr, 0, nullptr, 0, nullptr,
+                               &amax, sh);
+    }
+    const float g = grid_global_scale(amax, ws, g_out, status, 8);
+    if (g < 0.0f) return;
+    for (int64_t r0 = (int64_t)blockIdx.x * kRowsPerBlock; r0 < rows; r0 += (int64_t)gridDim.x * kRowsPerBlock) {
+        const int64_t row = r0 + rb;
+        const bool ok = row < rows;
+        row_share<NORM, true>(reinterpret_cast<const uint4*>(x + (ok ? row : 0) * ldx), row, ok, rb, q, nvec, cols,
+                              reinterpret_cast<const uint4*>(norm_w), eps, g, codes, ld_codes, sf, kb_pad, nullptr,
+                              nullptr, sh);
+    }
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_cooperative(void (*kernel)(KArgs...), unsigned grid, cudaStream_t stream, Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kRowThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+// Blocks of a kernel that can be resident on one SM at once.
+int blocks_per_sm(const void* kernel)
+{
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, kRowThreads, 0) != cudaSuccess) return 0;
+    return n;
+}
+
 }  // namespace
 
 cudaError_t launch_amax_scale(const __nv_bfloat16* x, int64_t rows, int64_t cols, int64_t ldx,
@@ -350,6 +554,47 @@ cudaError_t launch_finalize_scale(uint32_t* ws, float* g_out, cudaStream_t strea
 {
     finalize_scale_kernel<<<1, 1, 0, stream>>>(ws, g_out);
     return cudaGetLastError();
+}
+
+cudaError_t launch_scale_quantize(const __nv_bfloat16* x, int64_t rows, int64_t cols, int64_t ldx,
+                                  const __nv_bfloat16* norm_w, float eps, float* g_out, uint8_t* codes,
+                                  int64_t ld_codes, uint8_t* sf, uint32_t* ws, int* status, int num_sms,
+                                  cudaStream_t stream)
+{
+    // resident blocks per SM of the four kernels, per device
+    static int occ[64][4];
+    static bool have[64];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 64) return cudaErrorInvalidDevice;
+    if (!have[dev]) {
+        occ[dev][0] = blocks_per_sm((const void*)scale_quantize_resident_kernel<false>);
+        occ[dev][1] = blocks_per_sm((const void*)scale_quantize_resident_kernel<true>);
+        occ[dev][2] = blocks_per_sm((const void*)scale_quantize_kernel<false>);
+        occ[dev][3] = blocks_per_sm((const void*)scale_quantize_kernel<true>);
+        for (int i = 0; i < 4; i++)
+            if (occ[dev][i] < 1) return cudaErrorInvalidConfiguration;
+        have[dev] = true;
+    }
+    const bool norm = norm_w != nullptr;
+    const int64_t pairs = (rows + kRowsPerBlock - 1) / kRowsPerBlock;
+    const int64_t res_cap = (int64_t)occ[dev][norm ? 1 : 0] * num_sms;
+    if (cols <= kResMaxCols && pairs <= res_cap) {
+        const unsigned grid = (unsigned)pairs;
+        if (norm)
+            return launch_cooperative(scale_quantize_resident_kernel<true>, grid, stream, x, rows, cols, ldx, norm_w,
+                                      eps, g_out, codes, ld_codes, sf, ws, status);
+        return launch_cooperative(scale_quantize_resident_kernel<false>, grid, stream, x, rows, cols, ldx, norm_w,
+                                  eps, g_out, codes, ld_codes, sf, ws, status);
+    }
+    const int64_t cap = (int64_t)occ[dev][norm ? 3 : 2] * num_sms;
+    const unsigned grid = (unsigned)(pairs < cap ? pairs : cap);
+    if (norm)
+        return launch_cooperative(scale_quantize_kernel<true>, grid, stream, x, rows, cols, ldx, norm_w, eps, g_out,
+                                  codes, ld_codes, sf, ws, status);
+    return launch_cooperative(scale_quantize_kernel<false>, grid, stream, x, rows, cols, ldx, norm_w, eps, g_out,
+                              codes, ld_codes, sf, ws, status);
 }
 
 }  // namespace nvfp4

@@ -173,3 +173,50 @@ def test_deterministic(nv, ws):
     b = quantize_gpu(x, ws)
     torch.cuda.synchronize()
     assert torch.equal(a.codes, b.codes) and torch.equal(a.sf, b.sf) and torch.equal(a.g, b.g)
+
+
+# One-launch scale + quantize (cooperative kernel with a grid barrier).  The
+# shapes cover the resident variant (every row pair its own block, rows held
+# in registers) and the looping variant (more rows than resident blocks, or
+# rows wider than the register share), with and without the RMSNorm.
+FUSED = [(1, 64, False), (3, 128, True), (17, 320, False), (130, 1024, True), (777, 5120, True),
+         (1024, 5120, True), (1024, 5120, False), (1300, 5120, True), (5, 17408, True), (2500, 256, False)]
+
+
+@pytest.mark.parametrize("rows,cols,norm", FUSED)
+def test_scale_quantize_bit_exact(nv, ws, rows, cols, norm):
+    rng = np.random.default_rng(rows * 13 + cols)
+    x = synthetic.normal(rng, (rows, cols))
+    w = synthetic.norm_weight(cols + 1, cols) if norm else None
+    t = nv.NVFP4Tensor.empty(rows, cols)
+    nv.nvfp4_scale_quantize(dev(x), t, ws, None if w is None else dev(w), 1e-6)
+    v = oracle.rmsnorm(x, w, 1e-6) if norm else x
+    c, s, g = oracle_quant(v)
+    assert_same_quant(t, c, s, g, f"fused {rows}x{cols} norm={norm}")
+    assert nv.device_status() == 0
+    assert int(ws[:16].count_nonzero()) == 0          # barrier words back to zero
+
+
+@pytest.mark.parametrize("T,norm", [(777, True), (777, False), (3, True)])
+def test_scale_quantize_outliers_pitched_repeat(nv, ws, T, norm):
+    """Outlier activations read through a row pitch wider than the row;
+    two calls on one workspace agree bit for bit with each other, with the
+    two-launch path, and with the oracle."""
+    x = synthetic.activations(T, seed=6, outliers=True)
+    w = synthetic.norm_weight(19) if norm else None
+    wide = np.zeros((T, 5120 + 64), np.uint16)
+    wide[:, :5120] = x
+    xd = dev(wide)[:, :5120]
+    wd = None if w is None else dev(w)
+    a = nv.NVFP4Tensor.empty(T, 5120)
+    b = nv.NVFP4Tensor.empty(T, 5120)
+    nv.nvfp4_scale_quantize(xd, a, ws, wd, 1e-6)
+    nv.nvfp4_scale_quantize(xd, b, ws, wd, 1e-6)
+    two = nv.quantize_new(xd, ws, norm_w=wd)
+    torch.cuda.synchronize()
+    for o in (b, two):
+        assert torch.equal(a.codes, o.codes) and torch.equal(a.sf, o.sf) and torch.equal(a.g, o.g)
+    v = oracle.rmsnorm(x, w, 1e-6) if norm else x
+    c, s, g = oracle_quant(v)
+    assert_same_quant(a, c, s, g, f"fused outliers T={T} norm={norm}")
+    assert nv.device_status() == 0

@@ -131,7 +131,11 @@ int64_t sf_tile_stride(int64_t cols) { return pad_to(cols / 16, 4) / 4 * 512; }
 // one 128-row tile per CTA.  Over the prefill block's four GEMM shapes the
 // pair kernel is slower in sum (faster on the deep-K down projection, slower
 // on the others), so the threshold is set above any M.
+#ifdef NVFP4_PAIR_MIN_ROWS
+constexpr int64_t kPairMinRows = NVFP4_PAIR_MIN_ROWS;   // probe builds only
+#else
 constexpr int64_t kPairMinRows = INT64_MAX;
+#endif
 
 cudaError_t run_gemm(const CUtensorMap& ma, const CUtensorMap& mb0, const CUtensorMap& mb1, const GemmArgs& a,
                      const DeviceInfo* d, cudaStream_t stream)

@@ -57,15 +57,18 @@ static_assert(kAccCols + kStages * kSfColsPerStage <= kTmemCols, "tensor memory 
 // Warp roles (16 warps, 4 warpgroups): warps 0-3 and 5-7 are copy
 // producers (each a separate copy stream), warp 4 is the MMA warp, warps
 // 8-15 the epilogue.  Launched at 128 registers per thread; warpgroups 0-1
-// drop to 56 and warpgroups 2-3 rise to 200 (56 + 56 + 200 + 200 = 512 per
+// drop to 64 and warpgroups 2-3 rise to 192 (64 + 64 + 192 + 192 = 512 per
 // lane of each sub-partition, its 16384 registers).
 constexpr int kProducers = 7;
 constexpr int kMmaWarp = 4;
 constexpr int kEpiWarp0 = 8;
 constexpr int kEpiWarps = 8;
 constexpr int kNumThreads = 512;
-constexpr uint32_t kRegsSmall = 56;
-constexpr uint32_t kRegsEpi = 200;
+constexpr uint32_t kRegsSmall = 64;
+constexpr uint32_t kRegsEpi = 192;
+// Split fix-up: warps with at most this many valid rows fetch the partials
+// with their lanes spread over the columns instead of over the rows.
+constexpr int kFixRowsByLane = 4;
 static_assert(2 * kRegsSmall + 2 * kRegsEpi == 512, "register split per sub-partition");
 static_assert(kProducers == kEpiWarp0 - 1, "producers: warpgroups 0-1 less the MMA warp");
 
@@ -88,10 +91,10 @@ __device__ unsigned long long g_trace[1280];
 #define TRACE(slot, i) \
     do { if (blockIdx.x == NVFP4_TRACE_CTA && (i) < 64 * ((slot) < 1024 ? 4 : 1)) g_trace[(slot) + (i)] = clock64(); } while (0)
 // Per-CTA events on the global timer (ns): [c][0] start, [c][1] first
-// accumulator ready, [c][2] first segment's partial stored or tile
+// accumulator ready, [c][2] first segment's partial stored or first tile
 // finished, [c][3] last segment finished.
 __device__ unsigned long long g_trace_cta[256][4];
-__device__ unsigned long long g_trace_fix[16];   // CTA 0, first epilogue warp: [c] contributor c's flag seen, [0] partials added
+__device__ unsigned long long g_trace_fix[16];   // CTA 0, first epilogue warp: [1] all flags seen, [0] partials added
 #define TRACE_CTA(k) \
     do { if (blockIdx.x < 256) g_trace_cta[blockIdx.x][k] = globaltimer(); } while (0)
 #else
@@ -111,36 +114,47 @@ struct Ctrl {
 static_assert(sizeof(Ctrl) <= kCtrlBytes, "control block");
 
 // Work schedule of one CTA, walked as segments (tile, first K stage, end K
-// stage) by every role alike: whole tiles strided over the grid, or (split)
-// a contiguous range of the flattened (tile, K stage) units, CTA c taking
-// units [c*U/G, (c+1)*U/G) of U = tiles x stages on a grid of G CTAs.
+// stage) by every role alike, on a grid of G CTAs: whole tiles c, c + G, ...;
+// or (split, stream-K) a contiguous range of the flattened (tile, K stage)
+// units, CTA c taking [c*U/G, (c+1)*U/G) of U = tiles x stages.
+// (32-bit counts: the launcher keeps tiles x stages below 2^31.)
 struct Schedule {
-    int64_t next;     // whole tiles: next tile; split: next unit
-    int64_t end;      // split: end of this CTA's units
-    int64_t tiles;
+    int next;         // whole tiles: next tile; split: next unit
+    int end;          // split: end of this CTA's units
+    int tiles;
     int stages;       // K stages per tile
     bool split;
 };
 
-__device__ __forceinline__ int64_t split_first_unit(int64_t cta, int64_t units)
+__device__ __forceinline__ int split_first_unit(int64_t cta, int64_t units)
 {
-    return cta * units / gridDim.x;
+    return (int)(cta * units / gridDim.x);
 }
 
 __device__ __forceinline__ Schedule make_schedule(int64_t tiles, int stages, bool split)
 {
     Schedule sc;
-    sc.tiles = tiles;
+    sc.tiles = (int)tiles;
     sc.stages = stages;
     sc.split = split;
     if (split) {
         sc.next = split_first_unit(blockIdx.x, tiles * stages);
         sc.end = split_first_unit(blockIdx.x + 1, tiles * stages);
     } else {
-        sc.next = blockIdx.x;
+        sc.next = (int)blockIdx.x;
         sc.end = 0;
     }
     return sc;
+}
+
+// One past the last CTA holding a piece of the tile that the calling CTA
+// finishes (its contributors are the CTAs blockIdx.x + 1 .. end - 1).
+__device__ __forceinline__ int64_t finisher_end(const Schedule& sc, int64_t tile)
+{
+    const int64_t units = (int64_t)sc.tiles * sc.stages, tile_end = (tile + 1) * sc.stages;
+    int64_t c_end = (int64_t)blockIdx.x + 1;
+    while (c_end < (int64_t)gridDim.x && split_first_unit(c_end, units) < tile_end) c_end++;
+    return c_end;
 }
 
 __device__ __forceinline__ bool next_segment(Schedule& sc, int64_t& tile, int& ks, int& ke)
@@ -150,14 +164,15 @@ __device__ __forceinline__ bool next_segment(Schedule& sc, int64_t& tile, int& k
         tile = sc.next;
         ks = 0;
         ke = sc.stages;
-        sc.next += gridDim.x;
+        sc.next += (int)gridDim.x;
         return true;
     }
     if (sc.next >= sc.end) return false;
-    tile = sc.next / sc.stages;
-    ks = (int)(sc.next - tile * sc.stages);
-    const int64_t left = sc.end - sc.next;
-    ke = left < sc.stages - ks ? ks + (int)left : sc.stages;
+    const int t = sc.next / sc.stages;
+    tile = t;
+    ks = sc.next - t * sc.stages;
+    const int left = sc.end - sc.next;
+    ke = left < sc.stages - ks ? ks + left : sc.stages;
     sc.next += ke - ks;
     return true;
 }
@@ -176,15 +191,15 @@ __device__ __forceinline__ int flag_get_relaxed(const int* f)
     return v;
 }
 
-// Warp-wide bounded wait (converged: every lane polls, a vote decides) for a
-// ready flag; gives up like mbar_wait_warp.  The polls are relaxed: the
-// caller orders its reads of the flagged data after the wait with one
-// acquire fence.
+// Warp-wide bounded wait (converged: every lane polls its own ready flag,
+// or none when f is null, and a vote decides); gives up like mbar_wait_warp.
+// The polls are relaxed: the caller orders its reads of the flagged data
+// after the wait with one acquire fence.
 __device__ __forceinline__ bool flag_wait_warp(const int* f, volatile int* abort_flag, int* status, int site)
 {
     const uint64_t t0 = clock64();
     for (uint32_t i = 0;; i++) {
-        if (__all_sync(0xffffffffu, flag_get_relaxed(f) != 0)) return true;
+        if (__all_sync(0xffffffffu, f == nullptr || flag_get_relaxed(f) != 0)) return true;
         if ((i & 255u) == 255u) {
             int stop = *abort_flag ? 1 : ((uint64_t)(clock64() - t0) > kWaitLimitCycles ? 2 : 0);
             stop = __shfl_sync(0xffffffffu, stop, 0);
@@ -512,19 +527,60 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 // first K stages of a tile whose later stages other CTAs
                 // hold (each as the first segment of its range): wait for
                 // their partials, add them, then return their flags to zero
-                const int64_t units = num_tiles * num_kstages, tile_end = (tile + 1) * num_kstages;
-                int64_t c_end = (int64_t)blockIdx.x + 1;
-                while (c_end < (int64_t)gridDim.x && split_first_unit(c_end, units) < tile_end) c_end++;
+                const int64_t c_end = finisher_end(sched, tile);
+                // lane i waits for contributor blockIdx.x + 1 + i (+ 32k)
                 bool got = true;
-                for (int64_t c = (int64_t)blockIdx.x + 1; c < c_end && got; c++) {
-                    got = flag_wait_warp(args.sk_flags + c * kSplitFlagsPerCta + we, abort_flag, args.status, 5);
-#ifdef NVFP4_TRACE
-                    if (blockIdx.x == 0 && warp == kEpiWarp0 && lane == 0 && c < 16) g_trace_fix[c] = globaltimer();
-#endif
+                for (int64_t cb = (int64_t)blockIdx.x + 1; cb < c_end && got; cb += 32) {
+                    const int64_t c = cb + lane;
+                    got = flag_wait_warp(c < c_end ? args.sk_flags + c * kSplitFlagsPerCta + we : nullptr, abort_flag,
+                                         args.status, 5);
                 }
+#ifdef NVFP4_TRACE
+                if (blockIdx.x == 0 && warp == kEpiWarp0 && lane == 0) g_trace_fix[1] = globaltimer();
+#endif
                 if (!got) break;
                 asm volatile("fence.acq_rel.gpu;" ::: "memory");
-                if (row < args.M) {
+                const int64_t wrow0 = mt * 128 + q * 32;             // first row of this warp
+                const int nrows = (int)(args.M - wrow0 < 32 ? (args.M - wrow0 > 0 ? args.M - wrow0 : 0) : 32);
+                if (nrows > 0 && nrows <= kFixRowsByLane) {
+                    // few rows (decode): lane j fetches the 4 columns 4j..4j+3
+                    // of each row from up to 4 partials at once, sums them
+                    // in CTA order and hands them to the row's lane
+                    for (int rr = 0; rr < nrows; rr++) {
+                        float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                        for (int64_t c0 = (int64_t)blockIdx.x + 1; c0 < c_end; c0 += 4) {
+                            float4 t[4];
+#pragma unroll
+                            for (int i = 0; i < 4; i++)
+                                t[i] = c0 + i < c_end ? __ldcg(reinterpret_cast<const float4*>(
+                                                                   args.sk_partials + (c0 + i) * kSplitSlotFloats) +
+                                                               we * 1024 + lane * 32 + rr)
+                                                         : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+#pragma unroll
+                            for (int i = 0; i < 4; i++) {
+                                if (c0 + i < c_end) {
+                                    acc.x += t[i].x;
+                                    acc.y += t[i].y;
+                                    acc.z += t[i].z;
+                                    acc.w += t[i].w;
+                                }
+                            }
+                        }
+#pragma unroll
+                        for (int j = 0; j < 32; j++) {
+                            const float ax = __shfl_sync(0xffffffffu, acc.x, j);
+                            const float ay = __shfl_sync(0xffffffffu, acc.y, j);
+                            const float az = __shfl_sync(0xffffffffu, acc.z, j);
+                            const float aw = __shfl_sync(0xffffffffu, acc.w, j);
+                            if (lane == rr) {
+                                v[4 * j] += ax;
+                                v[4 * j + 1] += ay;
+                                v[4 * j + 2] += az;
+                                v[4 * j + 3] += aw;
+                            }
+                        }
+                    }
+                } else if (row < args.M) {
                     for (int64_t c = (int64_t)blockIdx.x + 1; c < c_end; c++) {
                         const float4* slot =
                             reinterpret_cast<const float4*>(args.sk_partials + c * kSplitSlotFloats) + we * 1024 + lane;
@@ -547,11 +603,12 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 #ifdef NVFP4_TRACE
                 if (blockIdx.x == 0 && warp == kEpiWarp0 && lane == 0) g_trace_fix[0] = globaltimer();
 #endif
-                if (lane == 0)
-                    for (int64_t c = (int64_t)blockIdx.x + 1; c < c_end; c++) args.sk_flags[c * kSplitFlagsPerCta + we] = 0;
+                for (int64_t c = (int64_t)blockIdx.x + 1 + lane; c < c_end; c += 32)
+                    args.sk_flags[c * kSplitFlagsPerCta + we] = 0;
                 if (warp == kEpiWarp0 && lane == 0) TRACE(1216, ecount - 1);
             }
             epilogue_row(args, swiglu, v, row, nt, h, alpha0, alpha1, g_inter, wamax);
+            if (warp == kEpiWarp0 && lane == 0 && ecount == 1) TRACE_CTA(2);
             if (warp == kEpiWarp0 && lane == 0) TRACE_CTA(3);
         }
         if (args.epilogue == kEpiSwigluBf16) {
@@ -601,9 +658,14 @@ cudaError_t launch_gemm(const CUtensorMap& map_a, const CUtensorMap& map_b0, con
     // K >= 8192) repay; spreading shallow tiles over all SMs also makes
     // every CTA stream its own weight slab, which defeats the L2 sharing of
     // concurrently running whole tiles.
+    // (Splitting the partial last wave of shallow-K tiles over the idle SMs
+    // was measured slower: each CTA streams its K stages at a rate set by
+    // its own load latency, so the idle SMs buy little, and the partials
+    // and the split instantiation cost more.)
     const int64_t waves = (tiles + num_sms - 1) / num_sms;
     const bool split = args.sk_partials != nullptr && args.sk_flags != nullptr && num_sms <= kSplitMaxCtas &&
-                       tiles * stages >= num_sms && tiles * 10 < waves * num_sms * 9 && stages >= 32;
+                       tiles * stages >= num_sms && tiles * 10 < waves * num_sms * 9 && stages >= 32 &&
+                       tiles * stages < (int64_t)1 << 31;
     if (split)
         gemm_kernel<true><<<(unsigned)num_sms, kNumThreads, kSmemBytes, stream>>>(map_a, map_b0, map_b1, args);
     else

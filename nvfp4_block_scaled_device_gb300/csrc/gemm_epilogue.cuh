@@ -25,30 +25,44 @@ __device__ __forceinline__ void epilogue_row(const GemmArgs& args, bool swiglu, 
             const int64_t n_base = nt * 256 + h * 128;
             __nv_bfloat16* orow = args.out + row * args.ldo;
             const __nv_bfloat16* rrow = args.residual ? args.residual + row * args.ldr : nullptr;
+            // Eight 16-byte vectors per batch: the batch's residual loads are
+            // all issued before its stores.  The output may alias the
+            // residual only element for element (same pitch), and each
+            // thread reads exactly the residual elements it then overwrites,
+            // so the early loads see the values the stores replace.
 #pragma unroll
-            for (int j = 0; j < 128; j += 8) {
-                const int64_t n = n_base + j;
-                if (n < args.N) {
-                    float y[8];
+            for (int jb = 0; jb < 128; jb += 64) {
+                uint4 rp[8];
 #pragma unroll
-                    for (int i = 0; i < 8; i++) y[i] = bf16_round(__fmul_rn(v[j + i], alpha0));
-                    if (rrow) {
-                        const uint4 rp = *reinterpret_cast<const uint4*>(rrow + n);
-                        y[0] = __fadd_rn(bf16_lo(rp.x), y[0]);
-                        y[1] = __fadd_rn(bf16_hi(rp.x), y[1]);
-                        y[2] = __fadd_rn(bf16_lo(rp.y), y[2]);
-                        y[3] = __fadd_rn(bf16_hi(rp.y), y[3]);
-                        y[4] = __fadd_rn(bf16_lo(rp.z), y[4]);
-                        y[5] = __fadd_rn(bf16_hi(rp.z), y[5]);
-                        y[6] = __fadd_rn(bf16_lo(rp.w), y[6]);
-                        y[7] = __fadd_rn(bf16_hi(rp.w), y[7]);
+                for (int t = 0; t < 8; t++) {
+                    const int64_t n = n_base + jb + 8 * t;
+                    rp[t] = (rrow && n < args.N) ? *reinterpret_cast<const uint4*>(rrow + n) : make_uint4(0, 0, 0, 0);
+                }
+#pragma unroll
+                for (int t = 0; t < 8; t++) {
+                    const int j = jb + 8 * t;
+                    const int64_t n = n_base + j;
+                    if (n < args.N) {
+                        float y[8];
+#pragma unroll
+                        for (int i = 0; i < 8; i++) y[i] = bf16_round(__fmul_rn(v[j + i], alpha0));
+                        if (rrow) {
+                            y[0] = __fadd_rn(bf16_lo(rp[t].x), y[0]);
+                            y[1] = __fadd_rn(bf16_hi(rp[t].x), y[1]);
+                            y[2] = __fadd_rn(bf16_lo(rp[t].y), y[2]);
+                            y[3] = __fadd_rn(bf16_hi(rp[t].y), y[3]);
+                            y[4] = __fadd_rn(bf16_lo(rp[t].z), y[4]);
+                            y[5] = __fadd_rn(bf16_hi(rp[t].z), y[5]);
+                            y[6] = __fadd_rn(bf16_lo(rp[t].w), y[6]);
+                            y[7] = __fadd_rn(bf16_hi(rp[t].w), y[7]);
+                        }
+                        uint4 o;
+                        o.x = pack_bf16x2(y[0], y[1]);
+                        o.y = pack_bf16x2(y[2], y[3]);
+                        o.z = pack_bf16x2(y[4], y[5]);
+                        o.w = pack_bf16x2(y[6], y[7]);
+                        *reinterpret_cast<uint4*>(orow + n) = o;
                     }
-                    uint4 o;
-                    o.x = pack_bf16x2(y[0], y[1]);
-                    o.y = pack_bf16x2(y[2], y[3]);
-                    o.z = pack_bf16x2(y[4], y[5]);
-                    o.w = pack_bf16x2(y[6], y[7]);
-                    *reinterpret_cast<uint4*>(orow + n) = o;
                 }
             }
         }

@@ -111,10 +111,10 @@ def test_deterministic(nv, ws):
     assert torch.equal(o1, o2)
 
 
-@pytest.mark.parametrize("M,N,K", [(1024, 7168, 5120), (1024, 5120, 17408), (1, 5120, 17408)])
+@pytest.mark.parametrize("M,N,K", [(1024, 7168, 5120), (1024, 5120, 5120), (1024, 5120, 17408), (1, 5120, 17408)])
 @pytest.mark.parametrize("split", [False, True])
 def test_full_size_sampled(nv, ws, M, N, K, split):
-    """Full projection sizes of the 27B-class model (QKV, down): quantized
+    """Full projection sizes of the 27B-class model (QKV, O, down): quantized
     operands compared in full, GEMM outputs on 2048 sampled elements; with and
     without the workspace that lets the GEMM split tiles over all SMs."""
     rng = np.random.default_rng(M + N)
@@ -140,12 +140,26 @@ def test_full_size_sampled(nv, ws, M, N, K, split):
 
 # Split schedule: the tiles' K ranges spread over all SMs, fp32 partials
 # combined through the workspace.  Deep-K shapes whose tiles leave most SMs
-# idle (so the split is taken), including a ragged M and a K with a partial
-# last stage (K = 8384: 32 full stages of 256 + 192).
-@pytest.mark.parametrize("M,N,K", [(777, 512, 8192), (300, 1024, 8192), (300, 768, 8384), (1, 5120, 8192)])
+# idle (so the split is taken), including a ragged M, a K with a partial
+# last stage (K = 8384: 32 full stages of 256 + 192), and tiles with only a
+# few valid rows (M = 1, 3, 131) whose partials are fetched column-wise, one
+# of them combining some 40 partials per tile.
+@pytest.mark.parametrize("M,N,K", [(777, 512, 8192), (300, 1024, 8192), (300, 768, 8384), (1, 5120, 8192),
+                                   (3, 1024, 16384), (131, 1024, 8192)])
 def test_split_schedule(nv, ws, M, N, K):
     got, ref, absref = run_case(nv, ws, M, N, K, seed=M + 7 * N + K, split=True)
     check_close(got, ref, absref, f"{M}x{N}x{K} split")
+
+
+# Shallow-K shapes with a partial last wave, called with a split workspace
+# (which the launcher leaves unused for them): residual epilogue, ragged M,
+# a K that ends in a partial stage (K = 2112: 8 stages of 256 + 64), tiles
+# with few valid rows.
+@pytest.mark.parametrize("M,N,K", [(1024, 5120, 5120), (128, 7168, 5120), (300, 2560, 2048), (130, 1024, 2112),
+                                   (3, 7168, 5120)])
+def test_partial_wave_with_workspace(nv, ws, M, N, K):
+    got, ref, absref = run_case(nv, ws, M, N, K, seed=M + 5 * N + K, residual=True, split=True)
+    check_close(got, ref, absref, f"{M}x{N}x{K} partial wave")
 
 
 def test_split_residual_and_repeat(nv, ws):

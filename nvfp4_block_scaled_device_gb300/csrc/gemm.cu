@@ -46,7 +46,9 @@ constexpr int kSfaBytes = 4 * kSfTile;         // 4 K-steps of 64
 constexpr int kSfbBytes = 8 * kSfTile;         // 2 row tiles x 4 K-steps
 constexpr int kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;  // 55296
 constexpr int kCtrlBytes = 256;
-constexpr int kSmemBytes = kStages * kStageBytes + kCtrlBytes + 1024;   // + alignment slack
+// ring, control block, the epilogue warps' bf16 staging areas, alignment slack
+constexpr int kSmemBytes = kStages * kStageBytes + kCtrlBytes + 8 * kEpiStageBytes + 1024;   // 8 epilogue warps
+static_assert(kSmemBytes <= 232448, "shared memory per block");
 
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCols = 256;
@@ -63,6 +65,7 @@ constexpr int kProducers = 7;
 constexpr int kMmaWarp = 4;
 constexpr int kEpiWarp0 = 8;
 constexpr int kEpiWarps = 8;
+static_assert(kEpiWarps == 8, "shared memory holds 8 epilogue staging areas");
 constexpr int kNumThreads = 512;
 constexpr uint32_t kRegsSmall = 64;
 constexpr uint32_t kRegsEpi = 192;
@@ -463,6 +466,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         setmaxnreg_inc<kRegsEpi>();                        // warpgroups 2-3
         const int q = warp & 3;             // tensor-memory lane quarter of this warp
         const int h = (warp - kEpiWarp0) >> 2;   // which half of the tile's columns
+        // this warp's bf16 staging area, after the ring and the control block
+        const uint32_t epi_stage = base + (uint32_t)(kStages * kStageBytes + kCtrlBytes) +
+                                   (uint32_t)((warp - kEpiWarp0) * kEpiStageBytes);
         const uint32_t lane_addr = tmem + ((uint32_t)(q * 32) << 16);
         const float ga = *args.ga;
         const float alpha0 = __fmul_rn(ga, *args.gb0);
@@ -607,7 +613,12 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     args.sk_flags[c * kSplitFlagsPerCta + we] = 0;
                 if (warp == kEpiWarp0 && lane == 0) TRACE(1216, ecount - 1);
             }
-            epilogue_row(args, swiglu, v, row, nt, h, alpha0, alpha1, g_inter, wamax);
+            // bf16 stores through the staging while later tiles accumulate;
+            // direct stores (lower latency) for the exposed last epilogue
+            // and in the split kernel (deep K: few, long segments)
+            const bool last = sched.next >= sched.tiles;   // whole tiles: no tile follows
+            epilogue_row(args, swiglu, v, row, nt, h, alpha0, alpha1, g_inter, wamax,
+                         (!kSplit && !last) ? epi_stage : 0u);
             if (warp == kEpiWarp0 && lane == 0 && ecount == 1) TRACE_CTA(2);
             if (warp == kEpiWarp0 && lane == 0) TRACE_CTA(3);
         }

@@ -38,7 +38,9 @@ constexpr int kSfaBytes = 4 * kSfTile;         // own rows, 4 K-steps of 64
 constexpr int kSfbBytes = 8 * kSfTile;         // both 128-row halves of B, 4 K-steps
 constexpr int kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;  // 38912
 constexpr int kCtrlBytes = 256;
-constexpr int kSmemBytes = kStages * kStageBytes + kCtrlBytes + 1024;
+// ring, control block, the epilogue warps' bf16 staging areas, alignment slack
+constexpr int kSmemBytes = kStages * kStageBytes + kCtrlBytes + 8 * kEpiStageBytes + 1024;   // 8 epilogue warps
+static_assert(kSmemBytes <= 232448, "shared memory per block");
 static_assert(kStageBytes % 1024 == 0, "stages keep 1024-byte alignment (128-byte swizzle atoms)");
 
 constexpr uint32_t kTmemCols = 512;
@@ -55,6 +57,7 @@ constexpr int kProducers = 7;
 constexpr int kMmaWarp = 4;
 constexpr int kEpiWarp0 = 8;
 constexpr int kEpiWarps = 8;
+static_assert(kEpiWarps == 8, "shared memory holds 8 epilogue staging areas");
 constexpr int kNumThreads = 512;
 constexpr uint32_t kRegsSmall = 56;
 constexpr uint32_t kRegsEpi = 200;
@@ -345,6 +348,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
         setmaxnreg_inc<kRegsEpi>();                        // warpgroups 2-3
         const int q = warp & 3;             // tensor-memory lane quarter of this warp
         const int h = (warp - kEpiWarp0) >> 2;   // which half of the tile's columns
+        // this warp's bf16 staging area, after the ring and the control block
+        const uint32_t epi_stage = base + (uint32_t)(kStages * kStageBytes + kCtrlBytes) +
+                                   (uint32_t)((warp - kEpiWarp0) * kEpiStageBytes);
         const uint32_t lane_addr = tmem + ((uint32_t)(q * 32) << 16);
         const uint32_t acc_empty_leader = map_to_cta(smem_u32(&ctrl->acc_empty), 0);
         const float ga = *args.ga;
@@ -375,7 +381,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
             if (lane == 0) mbar_arrive_remote(acc_empty_leader);
             acc_ph ^= 1u;
             const int64_t row = mt * 256 + rank * 128 + q * 32 + lane;
-            epilogue_row(args, swiglu, v, row, nt, h, alpha0, alpha1, g_inter, wamax);
+            // the last tile's epilogue is exposed: direct stores
+            epilogue_row(args, swiglu, v, row, nt, h, alpha0, alpha1, g_inter, wamax,
+                         tile + num_pairs < num_tiles ? epi_stage : 0u);
         }
         if (args.epilogue == kEpiSwigluBf16) {
 #pragma unroll

@@ -16,30 +16,56 @@ __device__ __forceinline__ float silu_mul(float gate, float up)
     return __fmul_rn(__fdividef(gate, __fadd_rn(1.0f, __expf(-gate))), up);
 }
 
+// bf16 output rows can go out through a per-warp shared-memory staging area
+// of kEpiStageRows rows: a thread holds one row's 128 columns, so storing
+// them straight from registers makes every warp store touch 32 rows, which
+// slows the loads of the tiles accumulating meanwhile; staged, each warp
+// store writes two whole 256-byte row segments.
+constexpr int kEpiStageRows = 4;
+constexpr int kEpiStageRowBytes = 256 + 16;            // padded: the 4 rows' 16-byte chunks hit distinct banks
+constexpr int kEpiStageBytes = kEpiStageRows * kEpiStageRowBytes;   // per epilogue warp
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, const uint4& v)
+{
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr)
+{
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr)
+                 : "memory");
+    return v;
+}
+
+// v: this thread's accumulator values; row: its output row (warp-converged
+// call: every lane of the warp, rows >= M included); stage: this warp's
+// kEpiStageBytes of shared memory (shared-space address), or 0 for the
+// direct bf16 stores (lower latency: for an epilogue nothing overlaps).
 __device__ __forceinline__ void epilogue_row(const GemmArgs& args, bool swiglu, float (&v)[128], int64_t row,
                                              int64_t nt, int h, float alpha0, float alpha1, float g_inter,
-                                             float& wamax)
+                                             float& wamax, uint32_t stage)
 {
-    if (!swiglu) {
+    if (!swiglu && stage == 0u) {
+        // direct: each thread stores its own row; four 16-byte vectors per
+        // batch, the batch's residual loads issued before its stores (an
+        // output aliasing the residual element for element is read by the
+        // thread that then overwrites it)
         if (row < args.M) {
             const int64_t n_base = nt * 256 + h * 128;
             __nv_bfloat16* orow = args.out + row * args.ldo;
             const __nv_bfloat16* rrow = args.residual ? args.residual + row * args.ldr : nullptr;
-            // Eight 16-byte vectors per batch: the batch's residual loads are
-            // all issued before its stores.  The output may alias the
-            // residual only element for element (same pitch), and each
-            // thread reads exactly the residual elements it then overwrites,
-            // so the early loads see the values the stores replace.
 #pragma unroll
-            for (int jb = 0; jb < 128; jb += 64) {
-                uint4 rp[8];
+            for (int jb = 0; jb < 128; jb += 32) {
+                uint4 rp[4];
 #pragma unroll
-                for (int t = 0; t < 8; t++) {
+                for (int t = 0; t < 4; t++) {
                     const int64_t n = n_base + jb + 8 * t;
                     rp[t] = (rrow && n < args.N) ? *reinterpret_cast<const uint4*>(rrow + n) : make_uint4(0, 0, 0, 0);
                 }
 #pragma unroll
-                for (int t = 0; t < 8; t++) {
+                for (int t = 0; t < 4; t++) {
                     const int j = jb + 8 * t;
                     const int64_t n = n_base + j;
                     if (n < args.N) {
@@ -65,6 +91,66 @@ __device__ __forceinline__ void epilogue_row(const GemmArgs& args, bool swiglu, 
                     }
                 }
             }
+        }
+    } else if (!swiglu) {
+        // staged: t = bf16(alpha * acc) of this lane's row, packed
+        uint32_t pk[64];
+#pragma unroll
+        for (int i = 0; i < 64; i++)
+            pk[i] = pack_bf16x2(bf16_round(__fmul_rn(v[2 * i], alpha0)), bf16_round(__fmul_rn(v[2 * i + 1], alpha0)));
+        const int lane = threadIdx.x & 31;
+        const int64_t row0 = row - lane;                 // the warp's first row
+        const int64_t n_base = nt * 256 + h * 128;
+        const int c = lane & 15;                         // 16-byte chunk (8 columns) of a staged row
+        const int64_t n = n_base + 8 * c;
+        constexpr int kRounds = 32 / kEpiStageRows;
+        constexpr int kPerRound = kEpiStageRows / 2;      // chunks a lane stores per round
+        constexpr int kAhead = 3;                          // rounds of residual loads in flight
+        // this lane's output chunk (round r, part hh): row
+        // row0 + kEpiStageRows * r + 2 * hh + lane / 16, columns n .. n + 7.
+        // Residual loads run kAhead rounds ahead of the stores (an output
+        // aliasing the residual element for element is read by the thread
+        // that later overwrites it, before it does).
+        auto chunk_row = [&](int r, int hh) { return row0 + kEpiStageRows * r + 2 * hh + (lane >> 4); };
+        auto load_res = [&](int r, int hh) {
+            const int64_t orow = chunk_row(r, hh);
+            return (args.residual && orow < args.M && n < args.N)
+                       ? *reinterpret_cast<const uint4*>(args.residual + orow * args.ldr + n)
+                       : make_uint4(0, 0, 0, 0);
+        };
+        uint4 rp[kAhead * kPerRound];
+#pragma unroll
+        for (int i = 0; i < kAhead * kPerRound; i++) rp[i] = load_res(i / kPerRound, i % kPerRound);
+#pragma unroll
+        for (int r = 0; r < kRounds; r++) {
+            if ((lane / kEpiStageRows) == r) {
+                const uint32_t dst = stage + (uint32_t)(lane % kEpiStageRows) * kEpiStageRowBytes;
+#pragma unroll
+                for (int j = 0; j < 16; j++)
+                    st_shared_v4(dst + 16u * j, make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]));
+            }
+            __syncwarp();
+#pragma unroll
+            for (int hh = 0; hh < kPerRound; hh++) {
+                const int rr = 2 * hh + (lane >> 4);      // staged row of this lane's chunk
+                const int64_t orow = chunk_row(r, hh);
+                const uint4 t = ld_shared_v4(stage + (uint32_t)rr * kEpiStageRowBytes + 16u * c);
+                const int slot = (r % kAhead) * kPerRound + hh;
+                if (orow < args.M && n < args.N) {
+                    uint4 o = t;
+                    if (args.residual) {
+                        // out = bf16(residual + t)
+                        const uint4 q = rp[slot];
+                        o.x = pack_bf16x2(__fadd_rn(bf16_lo(q.x), bf16_lo(t.x)), __fadd_rn(bf16_hi(q.x), bf16_hi(t.x)));
+                        o.y = pack_bf16x2(__fadd_rn(bf16_lo(q.y), bf16_lo(t.y)), __fadd_rn(bf16_hi(q.y), bf16_hi(t.y)));
+                        o.z = pack_bf16x2(__fadd_rn(bf16_lo(q.z), bf16_lo(t.z)), __fadd_rn(bf16_hi(q.z), bf16_hi(t.z)));
+                        o.w = pack_bf16x2(__fadd_rn(bf16_lo(q.w), bf16_lo(t.w)), __fadd_rn(bf16_hi(q.w), bf16_hi(t.w)));
+                    }
+                    *reinterpret_cast<uint4*>(args.out + orow * args.ldo + n) = o;
+                }
+                if (r + kAhead < kRounds) rp[slot] = load_res(r + kAhead, hh);
+            }
+            __syncwarp();
         }
     } else {
         const int64_t col0 = nt * 128 + h * 64;   // intermediate column of v[0]

@@ -127,20 +127,26 @@ int64_t sf_tile_stride(int64_t cols) { return pad_to(cols / 16, 4) / 4 * 512; }
         if ((expr) != cudaSuccess) return NVFP4_ERR_CUDA; \
     } while (0)
 
-// The SM-pair kernel (256-row tiles) takes M >= kPairMinRows; below that,
-// one 128-row tile per CTA.  Over the prefill block's four GEMM shapes the
-// pair kernel is slower in sum (faster on the deep-K down projection, slower
-// on the others), so the threshold is set above any M.
+// The SM-pair kernel (256 x 256 tiles on two SMs) takes M >= kPairMinRows
+// when its tiles fill at least one wave of SM pairs; otherwise the 1-SM
+// kernel (128 x 256 tiles, split schedule over all SMs when given a
+// workspace) runs.  With the weights streaming from HBM, as in a layer
+// block whose weights exceed L2, the pair kernel's smaller per-SM operand
+// stages (38 KB vs 54 KB for the same MMA work, five stages in flight
+// instead of four) cover more of the load latency: measured faster on
+// every GEMM of the prefill block but O.
 #ifdef NVFP4_PAIR_MIN_ROWS
 constexpr int64_t kPairMinRows = NVFP4_PAIR_MIN_ROWS;   // probe builds only
 #else
-constexpr int64_t kPairMinRows = INT64_MAX;
+constexpr int64_t kPairMinRows = 129;
 #endif
 
 cudaError_t run_gemm(const CUtensorMap& ma, const CUtensorMap& mb0, const CUtensorMap& mb1, const GemmArgs& a,
                      const DeviceInfo* d, cudaStream_t stream)
 {
-    if (a.M >= kPairMinRows) {
+    const bool swiglu = a.epilogue != kEpiBf16;
+    const int64_t pair_tiles = (a.M + 255) / 256 * (swiglu ? a.N / 128 : (a.N + 255) / 256);
+    if (a.M >= kPairMinRows && pair_tiles * 2 >= d->num_sms) {
         // the pair kernel fetches the scale tiles through tensor maps too
         CUtensorMap msa, msb0, msb1;
         if (make_sf_map(&msa, a.sfa, nvfp4_sf_bytes(a.M, a.K)) != NVFP4_OK ||

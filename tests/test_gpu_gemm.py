@@ -183,3 +183,34 @@ def test_split_residual_and_repeat(nv, ws):
     assert int(gws[:8192].count_nonzero()) == 0          # flags back to zero
     d = (o1.double() - o3.double()).abs()
     assert float(d.max()) <= 2 ** -7 * float(o3.double().abs().max()) + 1e-2
+
+
+# SM-pair kernel (256 x 256 tiles on two SMs, taken when its tiles fill a
+# wave of SM pairs): ragged M (the last pair tile partly or wholly past M in
+# one CTA of the pair), K with a partial last stage, residual epilogue;
+# outputs compared on 4096 sampled elements, always including the last rows
+# and columns.
+@pytest.mark.parametrize("M,N,K", [(777, 10240, 320), (300, 19456, 576), (1023, 9728, 1088)])
+def test_pair_kernel_ragged_sampled(nv, ws, M, N, K):
+    rng = np.random.default_rng(M * 3 + N + K)
+    a = synthetic.normal(rng, (M, K))
+    w = synthetic.normal(rng, (N, K), std=0.02)
+    r = synthetic.normal(rng, (M, N))
+    A, W = quantize_gpu(a, ws), quantize_gpu(w, ws)
+    out = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    nv.nvfp4_gemm(A, W, out, residual=dev(r))
+    torch.cuda.synchronize()
+    assert nv.device_status() == 0
+    ac, asf, ga = oracle_quant(a)
+    wc, wsf, gw = oracle_quant(w)
+    assert_same_quant(A, ac, asf, ga, "A")
+    assert_same_quant(W, wc, wsf, gw, "W")
+    m = rng.integers(0, M, 4096)
+    n = rng.integers(0, N, 4096)
+    m[:16] = M - 1
+    n[16:32] = N - 1
+    m[32:48] = M - 1 - np.arange(16)      # rows of the last 128-row half tile
+    dot, adot = oracle.dot_sampled(ac, asf, wc, wsf, m, n)
+    alpha = float(np.float32(np.float32(ga) * np.float32(gw)))
+    got = f64(host(out))[m, n]
+    check_close(got, alpha * dot + f64(r)[m, n], alpha * adot, f"{M}x{N}x{K} pair sampled")

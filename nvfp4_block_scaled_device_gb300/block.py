@@ -22,6 +22,8 @@ the O projection's input shape and statistics of a real attention output.
 
 Every launch is a libnvfp4 call; this module only holds buffers and
 sequences calls.  All buffers are allocated at construction.
+``HostPipeline`` runs the block on host-resident ubatches with the copies to
+and from the device overlapped with the neighbouring steps' compute.
 """
 from __future__ import annotations
 
@@ -100,3 +102,69 @@ class PrefillBlock:
         rec("dn1")
 
     EVENT_NAMES = ("qkv0", "qkv1", "o0", "o1", "mlp0", "gu0", "gu1", "dn1")
+
+
+class HostPipeline:
+    """PrefillBlock steps on host-resident (pinned) ubatches, with the copies
+    overlapped: two device input/output buffer pairs, each with its own
+    CUDA graph of ``PrefillBlock.forward``; the host->device copy of step
+    i + 1 and the device->host copy of step i - 1 run on their own streams
+    while step i computes on ``stream``.  Events order each buffer's reuse:
+    an input buffer is refilled only after the step that read it finished,
+    an output buffer is overwritten only after its copy to the host finished.
+
+    The block's internal buffers are shared by both graphs; the graphs run
+    one after the other on ``stream``."""
+
+    def __init__(self, blk: PrefillBlock, stream):
+        self.blk = blk
+        self.stream = stream
+        dev = blk.attn_norm.device
+        T, H = blk.T, blk.H
+        self.x = [torch.empty((T, H), dtype=torch.bfloat16, device=dev) for _ in range(2)]
+        self.out = [torch.empty((T, H), dtype=torch.bfloat16, device=dev) for _ in range(2)]
+        self.graphs = []
+        for b in range(2):
+            self.x[b].zero_()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                blk.forward(self.x[b], self.out[b], stream)
+            self.graphs.append(g)
+        self.h2d = torch.cuda.Stream(dev)
+        self.d2h = torch.cuda.Stream(dev)
+        self.in_ready = [torch.cuda.Event() for _ in range(2)]
+        self.step_done = [torch.cuda.Event() for _ in range(2)]
+        self.out_free = [torch.cuda.Event() for _ in range(2)]
+        self.steps = 0
+
+    def submit(self, x_host: torch.Tensor, out_host: torch.Tensor):
+        """Enqueue one step: x_host (pinned bf16 [T x H]) in, out_host out.
+        Returns at once; out_host is valid after ``wait()`` (or after the
+        event of a later step that follows it)."""
+        b = self.steps % 2
+        if self.steps >= 2:
+            self.h2d.wait_event(self.step_done[b])         # the step that read x[b] has finished
+        with torch.cuda.stream(self.h2d):
+            self.x[b].copy_(x_host, non_blocking=True)
+            self.in_ready[b].record(self.h2d)
+        self.stream.wait_event(self.in_ready[b])
+        if self.steps >= 2:
+            self.stream.wait_event(self.out_free[b])       # out[b] has reached the host
+        with torch.cuda.stream(self.stream):
+            self.graphs[b].replay()
+            self.step_done[b].record(self.stream)
+        self.d2h.wait_event(self.step_done[b])
+        with torch.cuda.stream(self.d2h):
+            out_host.copy_(self.out[b], non_blocking=True)
+            self.out_free[b].record(self.d2h)
+        self.steps += 1
+
+    def join(self):
+        """Make ``stream`` wait for every copy enqueued so far."""
+        for b in range(2):
+            if self.steps > b:
+                self.stream.wait_event(self.out_free[b])
+
+    def wait(self):
+        self.join()
+        self.stream.synchronize()

@@ -159,6 +159,22 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
         : "memory");
 }
 
+// Programmatic dependent launch.  A kernel launched with the
+// programmatic-serialization attribute may start while the previous kernel
+// of the stream is still running: griddep_wait() returns once that kernel
+// has completed and its memory operations are visible (at once without such
+// a dependency).  griddep_launch_dependents() lets the next kernel of the
+// stream be scheduled before this one completes.
+__device__ __forceinline__ void griddep_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void griddep_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map)
 {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");

@@ -270,6 +270,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     tc_fence_after();
     const uint32_t tmem = ctrl->tmem_base;
     if (threadIdx.x == 0) TRACE_CTA(0);
+    // the next kernel of the stream may be scheduled from here on (it waits
+    // for this one before touching its outputs)
+    griddep_launch_dependents();
 
     if (warp < kEpiWarp0) {
         // warpgroups 0-1: one register-budget instruction for all eight warps
@@ -290,6 +293,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             // stale shared memory only feeds accumulator rows >= M or columns
             // >= N, never stored.
             const int p = warp < kMmaWarp ? warp : warp - 1;
+            // The weight boxes (producers 2-5) do not depend on the previous
+            // kernel and start at once; A and the scale tiles (producers 0,
+            // 1, 6) wait for it to complete (programmatic launch).
+            if (p < 2 || p == 6) griddep_wait();
             const uint32_t full0 = smem_u32(&ctrl->full[0]);
             const uint32_t empty0 = smem_u32(&ctrl->empty[0]);
             constexpr uint32_t kBox = kCodeBoxRows * 128u;
@@ -464,6 +471,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     } else {
         // ------------------------------------------------------ epilogue
         setmaxnreg_inc<kRegsEpi>();                        // warpgroups 2-3
+        griddep_wait();                     // scales, residual, outputs: after the previous kernel
         const int q = warp & 3;             // tensor-memory lane quarter of this warp
         const int h = (warp - kEpiWarp0) >> 2;   // which half of the tile's columns
         // this warp's bf16 staging area, after the ring and the control block
@@ -677,12 +685,13 @@ cudaError_t launch_gemm(const CUtensorMap& map_a, const CUtensorMap& map_b0, con
     const bool split = args.sk_partials != nullptr && args.sk_flags != nullptr && num_sms <= kSplitMaxCtas &&
                        tiles * stages >= num_sms && tiles * 10 < waves * num_sms * 9 && stages >= 32 &&
                        tiles * stages < (int64_t)1 << 31;
+    // programmatic launch: the CTAs may start on SMs the previous kernel has
+    // left and fetch weights before it completes
     if (split)
-        gemm_kernel<true><<<(unsigned)num_sms, kNumThreads, kSmemBytes, stream>>>(map_a, map_b0, map_b1, args);
-    else
-        gemm_kernel<false><<<(unsigned)(tiles < num_sms ? tiles : num_sms), kNumThreads, kSmemBytes, stream>>>(
-            map_a, map_b0, map_b1, args);
-    return cudaGetLastError();
+        return launch_programmatic(gemm_kernel<true>, dim3((unsigned)num_sms), dim3(kNumThreads), kSmemBytes, stream,
+                                   map_a, map_b0, map_b1, args);
+    return launch_programmatic(gemm_kernel<false>, dim3((unsigned)(tiles < num_sms ? tiles : num_sms)),
+                               dim3(kNumThreads), kSmemBytes, stream, map_a, map_b0, map_b1, args);
 }
 
 }  // namespace nvfp4

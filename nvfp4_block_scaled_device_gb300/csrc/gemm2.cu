@@ -152,6 +152,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
     cluster_sync_all();   // both CTAs' barriers are initialised before any cross-CTA signal
     tc_fence_after();
     const uint32_t tmem = ctrl->tmem_base;
+    // the next kernel of the stream may be scheduled from here on (it waits
+    // for this one before touching its outputs)
+    griddep_launch_dependents();
 
     if (warp < kEpiWarp0) {
         // warpgroups 0-1: one register-budget instruction for all eight warps
@@ -173,6 +176,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
             // stages or of the next rows (or zero fill past the end), which no
             // MMA reads.
             const int p = warp < kMmaWarp ? warp : warp - 1;
+            // The weight boxes and scales (producers 2, 3, 5, 6) do not
+            // depend on the previous kernel and start at once; A and its
+            // scales (producers 0, 1, 4) wait for it to complete.
+            if (p < 2 || p == 4) griddep_wait();
             const uint32_t full_leader0 = map_to_cta(smem_u32(&ctrl->full[0]), 0);
             const uint32_t empty0 = smem_u32(&ctrl->empty[0]);
             constexpr uint32_t kBox = kCodeBoxRows * 128u;
@@ -346,6 +353,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
     } else {
         // ------------------------------------------------------ epilogue
         setmaxnreg_inc<kRegsEpi>();                        // warpgroups 2-3
+        griddep_wait();                     // scales, residual, outputs: after the previous kernel
         const int q = warp & 3;             // tensor-memory lane quarter of this warp
         const int h = (warp - kEpiWarp0) >> 2;   // which half of the tile's columns
         // this warp's bf16 staging area, after the ring and the control block
@@ -422,9 +430,10 @@ cudaError_t launch_gemm2(const CUtensorMap& map_a, const CUtensorMap& map_b0, co
     const int64_t num_n = swiglu ? args.N / 128 : (args.N + 255) / 256;
     const int64_t tiles = num_m * num_n;
     const int64_t pairs = tiles < num_sms / 2 ? tiles : num_sms / 2;
-    gemm2_kernel<<<(unsigned)(2 * pairs), kNumThreads, kSmemBytes, stream>>>(map_a, map_b0, map_b1, map_sfa,
-                                                                              map_sfb0, map_sfb1, args);
-    return cudaGetLastError();
+    // programmatic launch: the CTAs may start on SMs the previous kernel has
+    // left and fetch weights before it completes
+    return launch_programmatic(gemm2_kernel, dim3((unsigned)(2 * pairs)), dim3(kNumThreads), kSmemBytes, stream,
+                               map_a, map_b0, map_b1, map_sfa, map_sfb0, map_sfb1, args);
 }
 
 }  // namespace nvfp4

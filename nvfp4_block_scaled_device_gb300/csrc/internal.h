@@ -37,6 +37,26 @@ cudaError_t launch_quantize(const __nv_bfloat16* x, int64_t rows, int64_t cols, 
 // g_out = max(amax(ws), 1e-8) / 2688, and the amax word is reset to zero.
 cudaError_t launch_finalize_scale(uint32_t* ws, float* g_out, cudaStream_t stream);
 
+// Launch `kernel` on `stream` with the programmatic-serialization attribute:
+// it may start while the previous kernel of the stream still runs, and must
+// call griddep_wait() before touching anything that kernel writes or reads.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_programmatic(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                                Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // launch_amax_scale followed by launch_quantize in one cooperative launch
 // (bit-identical results); sf padding rows are zero-filled.  A barrier wait
 // that gives up records a timeout in *status.

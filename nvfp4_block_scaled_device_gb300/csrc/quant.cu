@@ -244,6 +244,7 @@ __global__ void __launch_bounds__(kRowThreads, 3) amax_scale_kernel(const __nv_b
                                                                  float eps, float* __restrict__ g_out,
                                                                  uint32_t* __restrict__ ws)
 {
+    griddep_launch_dependents();   // a following GEMM may be scheduled early
     __shared__ RowShared sh;
     const int64_t nvec = cols / 8;
     const int wib = threadIdx.x >> 5, rb = wib / kWarpsPerRow, q = wib % kWarpsPerRow;
@@ -285,6 +286,7 @@ __global__ void __launch_bounds__(kRowThreads, 3) quantize_kernel(const __nv_bfl
                                                                uint8_t* __restrict__ sf,
                                                                __nv_bfloat16* __restrict__ y_out)
 {
+    griddep_launch_dependents();   // a following GEMM may be scheduled early
     __shared__ RowShared sh;
     const float g = *g_ptr;
     const int64_t nvec = cols / 8;          // a multiple of 8: cols % 64 == 0
@@ -399,6 +401,7 @@ __global__ void __launch_bounds__(kRowThreads, 4)
                                    uint8_t* __restrict__ codes, int64_t ld_codes, uint8_t* __restrict__ sf,
                                    uint32_t* __restrict__ ws, int* status)
 {
+    griddep_launch_dependents();   // a following GEMM may be scheduled early
     __shared__ RowShared sh;
     const int64_t nvec = cols / 8;
     const int64_t kb_pad = cols / 16;
@@ -469,6 +472,7 @@ __global__ void __launch_bounds__(kRowThreads, 3)
                           uint8_t* __restrict__ codes, int64_t ld_codes, uint8_t* __restrict__ sf,
                           uint32_t* __restrict__ ws, int* status)
 {
+    griddep_launch_dependents();   // a following GEMM may be scheduled early
     __shared__ RowShared sh;
     const int64_t nvec = cols / 8;
     const int64_t kb_pad = cols / 16;

@@ -94,6 +94,112 @@ struct Ctrl {
 };
 static_assert(sizeof(Ctrl) <= kCtrlBytes, "control block");
 
+// Work schedule of one SM pair, walked as segments (tile, first K stage, end
+// K stage) by every role of both CTAs alike, P pairs: whole tiles p, p + P,
+// ...; or (split, stream-K) the contiguous run [p*U/P, (p+1)*U/P) of the
+// U = tiles x stages flattened (tile, K stage) units, a tile split between
+// pairs being finished by the pair holding its first K stage.  (32-bit
+// counts: the launcher keeps tiles x stages below 2^31.)
+struct PairSchedule {
+    int next;         // whole tiles: next tile; split: next unit
+    int end;          // split: end of this pair's units
+    int tiles;
+    int stages;       // K stages per tile
+    int pairs;
+    bool split;
+};
+
+__device__ __forceinline__ int pair_first_unit(int64_t pair, int64_t units, int64_t pairs)
+{
+    return (int)(pair * units / pairs);
+}
+
+__device__ __forceinline__ PairSchedule make_pair_schedule(int64_t pair, int64_t pairs, int64_t tiles, int stages,
+                                                          bool split)
+{
+    PairSchedule sc;
+    sc.tiles = (int)tiles;
+    sc.stages = stages;
+    sc.pairs = (int)pairs;
+    sc.split = split;
+    if (split) {
+        sc.next = pair_first_unit(pair, tiles * stages, pairs);
+        sc.end = pair_first_unit(pair + 1, tiles * stages, pairs);
+    } else {
+        sc.next = (int)pair;
+        sc.end = 0;
+    }
+    return sc;
+}
+
+__device__ __forceinline__ bool next_pair_segment(PairSchedule& sc, int64_t& tile, int& ks, int& ke)
+{
+    if (!sc.split) {
+        if (sc.next >= sc.tiles) return false;
+        tile = sc.next;
+        ks = 0;
+        ke = sc.stages;
+        sc.next += sc.pairs;
+        return true;
+    }
+    if (sc.next >= sc.end) return false;
+    const int t = sc.next / sc.stages;
+    tile = t;
+    ks = sc.next - t * sc.stages;
+    const int left = sc.end - sc.next;
+    ke = left < sc.stages - ks ? ks + left : sc.stages;
+    sc.next += ke - ks;
+    return true;
+}
+
+// One past the last pair holding a piece of the tile that `pair` finishes
+// (its contributors are pairs pair + 1 .. end - 1).
+__device__ __forceinline__ int64_t pair_finisher_end(const PairSchedule& sc, int64_t pair, int64_t tile)
+{
+    const int64_t units = (int64_t)sc.tiles * sc.stages, tile_end = (tile + 1) * sc.stages;
+    int64_t e = pair + 1;
+    while (e < sc.pairs && pair_first_unit(e, units, sc.pairs) < tile_end) e++;
+    return e;
+}
+
+__device__ __forceinline__ void flag_set_release2(int* f, int v)
+{
+    asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(f), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ int flag_get_relaxed2(const int* f)
+{
+    int v;
+    asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
+    return v;
+}
+
+// Warp-wide bounded wait (every lane polls its own ready flag, or none when
+// f is null; a vote decides); gives up like mbar_wait_warp.  Relaxed polls:
+// the caller orders its reads of the flagged data with one acquire fence.
+__device__ __forceinline__ bool flag_wait_warp2(const int* f, volatile int* abort_flag, int* status, int site)
+{
+    const uint64_t t0 = clock64();
+    for (uint32_t i = 0;; i++) {
+        if (__all_sync(0xffffffffu, f == nullptr || flag_get_relaxed2(f) != 0)) return true;
+        if ((i & 255u) == 255u) {
+            int stop = *abort_flag ? 1 : ((uint64_t)(clock64() - t0) > kWaitLimitCycles ? 2 : 0);
+            stop = __shfl_sync(0xffffffffu, stop, 0);
+            if (stop != 0) {
+                if (stop == 2 && (threadIdx.x & 31) == 0) {
+                    *abort_flag = 1;
+                    if (status) atomicCAS(status, 0, kErrTimeout * 100 + site);
+                }
+                __syncwarp();
+                return false;
+            }
+        }
+    }
+}
+
+// kSplit: the split schedule (its fix-up code is compiled into this
+// instantiation only).
+template <bool kSplit>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
     gemm2_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b0,
                  const __grid_constant__ CUtensorMap map_b1, const __grid_constant__ CUtensorMap map_sfa,
@@ -192,7 +298,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
             uint32_t ph = 0;
             bool ok = true;
             int kcount = 0;
-            for (int64_t tile = pair; tile < num_tiles && ok; tile += num_pairs) {
+            PairSchedule sched = make_pair_schedule(pair, num_pairs, num_tiles, num_kstages, kSplit);
+            int64_t tile;
+            int ks, ke;
+            while (ok && next_pair_segment(sched, tile, ks, ke)) {
                 const int64_t mt = tile % num_m, nt = tile / num_m;
                 const int64_t row0 = mt * 256 + rank * 128;          // this CTA's first A row
                 int32_t yb;
@@ -229,7 +338,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
                         tx += kSfBox * ((r0 < args.M) + 1 + (has_b1 ? 1 : 0));
                     }
                 }
-                for (int kb = 0; kb < num_kstages; kb++) {
+                for (int kb = ks; kb < ke; kb++) {
                     if (!mbar_wait_cluster_warp(empty0 + 8u * (uint32_t)s, ph ^ 1u, abort_flag, args.status, 11)) {
                         ok = false;
                         break;
@@ -272,12 +381,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
                 uint32_t ph = 0, acc_ph = 0;
                 bool ok = true;
                 int kcount = 0;
-                for (int64_t tile = pair; tile < num_tiles && ok; tile += num_pairs) {
+                PairSchedule sched = make_pair_schedule(pair, num_pairs, num_tiles, num_kstages, kSplit);
+                int64_t tile;
+                int ks, ke;
+                while (ok && next_pair_segment(sched, tile, ks, ke)) {
                     if (!mbar_wait_cluster_warp(smem_u32(&ctrl->acc_empty), acc_ph ^ 1u, abort_flag, args.status, 12))
                         break;
                     tc_fence_after();
                     // full stages: nothing but the wait and one fused issue block
-                    for (int kb = 0; kb < full_kstages; kb++) {
+                    const int kb_full_end = ke < full_kstages ? ke : full_kstages;
+                    for (int kb = ks; kb < kb_full_end; kb++) {
                         if (!mbar_wait_cluster_warp(full0 + 8u * (uint32_t)s, ph, abort_flag, args.status, 13)) {
                             ok = false;
                             break;
@@ -288,7 +401,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
                         const uint32_t a_lo = desc_a_lo + soff;
                         stage_issue_2sm(tmem, tmem + kAccCols + (uint32_t)s * kSfColsPerStage, desc_sf_lo + soff,
                                         desc_sf_hi, a_lo, a_lo + (kABytes >> 4), desc_sw_hi, kIdesc2,
-                                        kb != 0 ? 1u : 0u, empty0 + 8u * (uint32_t)s, kPairMask);
+                                        kb != ks ? 1u : 0u, empty0 + 8u * (uint32_t)s, kPairMask);
                         TRACE2(1536, kcount);
                         kcount++;
                         if (++s == kStages) {
@@ -296,7 +409,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
                             ph ^= 1u;
                         }
                     }
-                    if (ok && tail_kk != 0) {
+                    if (ok && ke > full_kstages) {
                         // K tail: a last stage of fewer than 4 K-steps
                         if (!mbar_wait_cluster_warp(full0 + 8u * (uint32_t)s, ph, abort_flag, args.status, 13)) {
                             ok = false;
@@ -318,7 +431,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
                                 const uint32_t c = sf_stage + (uint32_t)kk * kSfColsPerKK;
                                 mma2_mxf4nvf4_warp(tmem, desc_from(a_lo + 2u * kk, desc_sw_hi),
                                                    desc_from(b_lo + 2u * kk, desc_sw_hi), kIdesc2, c, c + 4,
-                                                   (full_kstages | kk) != 0 ? 1u : 0u);
+                                                   (full_kstages != ks || kk != 0) ? 1u : 0u);
                             }
                             // the stage is free in both CTAs once these MMAs complete
                             mma_commit2_mc_warp(empty0 + 8u * (uint32_t)s, kPairMask);
@@ -367,7 +480,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
         const float g_inter = args.epilogue == kEpiSwigluFp4 ? *args.g_inter : 1.0f;
         uint32_t acc_ph = 0;
         float wamax = 0.0f;
-        for (int64_t tile = pair; tile < num_tiles; tile += num_pairs) {
+        const int we = warp - kEpiWarp0;   // epilogue warp index (its slice of a partial slot)
+        PairSchedule sched = make_pair_schedule(pair, num_pairs, num_tiles, num_kstages, kSplit);
+        int64_t tile;
+        int ks, ke;
+        while (next_pair_segment(sched, tile, ks, ke)) {
             const int64_t mt = tile % num_m, nt = tile / num_m;
             if (!mbar_wait_cluster_warp<true>(smem_u32(&ctrl->acc_full), acc_ph, abort_flag, args.status, 16)) break;
             tc_fence_after();
@@ -389,9 +506,65 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
             if (lane == 0) mbar_arrive_remote(acc_empty_leader);
             acc_ph ^= 1u;
             const int64_t row = mt * 256 + rank * 128 + q * 32 + lane;
-            // the last tile's epilogue is exposed: direct stores
+            if (kSplit && ks != 0) {
+                // later K stages of a tile finished by another pair: this
+                // warp's 32 x 128 partial into the CTA's slot (values
+                // 4j..4j+3 of lane l as one 16-byte vector at [we][j][l]),
+                // then its ready flag (release: after the warp's stores)
+                float4* slot = reinterpret_cast<float4*>(args.sk_partials + (int64_t)blockIdx.x * kSplitSlotFloats) +
+                               we * 1024 + lane;
+                if (row < args.M) {
+#pragma unroll
+                    for (int j = 0; j < 32; j++)
+                        __stcg(slot + j * 32, make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
+                }
+                __syncwarp();
+                if (lane == 0) flag_set_release2(args.sk_flags + blockIdx.x * kSplitFlagsPerCta + we, 1);
+                continue;
+            }
+            if (kSplit && ke != num_kstages) {
+                // first K stages of a tile whose later stages other pairs
+                // hold: wait for the partials of this CTA's rank in those
+                // pairs (lane i polls pair + 1 + i (+ 32k)), add them in pair
+                // order, return their flags to zero
+                const int64_t p_end = pair_finisher_end(sched, pair, tile);
+                bool got = true;
+                for (int64_t cb = pair + 1; cb < p_end && got; cb += 32) {
+                    const int64_t c = cb + lane;
+                    got = flag_wait_warp2(c < p_end ? args.sk_flags + (2 * c + rank) * kSplitFlagsPerCta + we : nullptr,
+                                          abort_flag, args.status, 17);
+                }
+                if (!got) break;
+                asm volatile("fence.acq_rel.gpu;" ::: "memory");
+                if (row < args.M) {
+                    for (int64_t c = pair + 1; c < p_end; c++) {
+                        const float4* slot = reinterpret_cast<const float4*>(args.sk_partials +
+                                                                             (2 * c + rank) * kSplitSlotFloats) +
+                                             we * 1024 + lane;
+#pragma unroll
+                        for (int jb = 0; jb < 32; jb += 16) {   // 16 loads in flight, then their adds
+                            float4 t[16];
+#pragma unroll
+                            for (int j = 0; j < 16; j++) t[j] = __ldcg(slot + (jb + j) * 32);
+#pragma unroll
+                            for (int j = 0; j < 16; j++) {
+                                v[4 * (jb + j)] += t[j].x;
+                                v[4 * (jb + j) + 1] += t[j].y;
+                                v[4 * (jb + j) + 2] += t[j].z;
+                                v[4 * (jb + j) + 3] += t[j].w;
+                            }
+                        }
+                    }
+                }
+                __syncwarp();
+                for (int64_t c = pair + 1 + lane; c < p_end; c += 32)
+                    args.sk_flags[(2 * c + rank) * kSplitFlagsPerCta + we] = 0;
+            }
+            // staged bf16 stores while later tiles accumulate; direct stores
+            // for the exposed last epilogue and in the split kernel
+            const bool last = sched.next >= sched.tiles;   // whole tiles: no tile follows
             epilogue_row(args, swiglu, v, row, nt, h, alpha0, alpha1, g_inter, wamax,
-                         tile + num_pairs < num_tiles ? epi_stage : 0u);
+                         (!kSplit && !last) ? epi_stage : 0u);
         }
         if (args.epilogue == kEpiSwigluBf16) {
 #pragma unroll
@@ -421,7 +594,9 @@ cudaError_t launch_gemm2(const CUtensorMap& map_a, const CUtensorMap& map_b0, co
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 64 && !attr_set_for_device[dev]) {
-        e = cudaFuncSetAttribute(gemm2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        e = cudaFuncSetAttribute(gemm2_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(gemm2_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
         if (e != cudaSuccess) return e;
         attr_set_for_device[dev] = 1;
     }
@@ -429,10 +604,23 @@ cudaError_t launch_gemm2(const CUtensorMap& map_a, const CUtensorMap& map_b0, co
     const int64_t num_m = (args.M + 255) / 256;
     const int64_t num_n = swiglu ? args.N / 128 : (args.N + 255) / 256;
     const int64_t tiles = num_m * num_n;
-    const int64_t pairs = tiles < num_sms / 2 ? tiles : num_sms / 2;
+    const int64_t stages = (args.K / 64 + 3) / 4;
+    const int64_t all_pairs = num_sms / 2;
+    // Whole tiles strided over min(tiles, pairs) pairs, unless (given a
+    // workspace) their last wave leaves more than a tenth of the pairs idle
+    // and the tiles are deep in K (>= 32 stages): then every pair takes an
+    // equal run of the (tile, K stage) units, as the 1-SM kernel's split.
+    const int64_t waves = (tiles + all_pairs - 1) / all_pairs;
+    const bool split = args.sk_partials != nullptr && args.sk_flags != nullptr && num_sms <= kSplitMaxCtas &&
+                       tiles * stages >= all_pairs && tiles * 10 < waves * all_pairs * 9 && stages >= 32 &&
+                       tiles * stages < (int64_t)1 << 31;
+    const int64_t pairs = split ? all_pairs : (tiles < all_pairs ? tiles : all_pairs);
     // programmatic launch: the CTAs may start on SMs the previous kernel has
     // left and fetch weights before it completes
-    return launch_programmatic(gemm2_kernel, dim3((unsigned)(2 * pairs)), dim3(kNumThreads), kSmemBytes, stream,
+    if (split)
+        return launch_programmatic(gemm2_kernel<true>, dim3((unsigned)(2 * pairs)), dim3(kNumThreads), kSmemBytes,
+                                   stream, map_a, map_b0, map_b1, map_sfa, map_sfb0, map_sfb1, args);
+    return launch_programmatic(gemm2_kernel<false>, dim3((unsigned)(2 * pairs)), dim3(kNumThreads), kSmemBytes, stream,
                                map_a, map_b0, map_b1, map_sfa, map_sfb0, map_sfb1, args);
 }
 

@@ -214,3 +214,35 @@ def test_pair_kernel_ragged_sampled(nv, ws, M, N, K):
     alpha = float(np.float32(np.float32(ga) * np.float32(gw)))
     got = f64(host(out))[m, n]
     check_close(got, alpha * dot + f64(r)[m, n], alpha * adot, f"{M}x{N}x{K} pair sampled")
+
+
+# Split schedule on SM pairs: deep K (>= 32 stages) with a partial last wave
+# of pair tiles, so the pairs share the (tile, K stage) units; ragged M, a K
+# with a partial last stage (K = 8384: 32 full stages of 256 + 192), residual;
+# two calls on one workspace agree bit for bit and leave its flags zero.
+@pytest.mark.parametrize("M,N,K", [(777, 5120, 8384), (1024, 5120, 17408)])
+def test_pair_split_sampled(nv, ws, M, N, K):
+    rng = np.random.default_rng(M + 11 * N + K)
+    a = synthetic.normal(rng, (M, K))
+    w = synthetic.normal(rng, (N, K), std=0.02)
+    r = synthetic.normal(rng, (M, N))
+    A, W = quantize_gpu(a, ws), quantize_gpu(w, ws)
+    gws = nv.workspace(nv.gemm_workspace_bytes())
+    o1 = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    o2 = torch.empty_like(o1)
+    nv.nvfp4_gemm(A, W, o1, residual=dev(r), workspace=gws)
+    nv.nvfp4_gemm(A, W, o2, residual=dev(r), workspace=gws)
+    torch.cuda.synchronize()
+    assert nv.device_status() == 0
+    assert torch.equal(o1, o2)
+    assert int(gws[:8192].count_nonzero()) == 0
+    ac, asf, ga = oracle_quant(a)
+    wc, wsf, gw = oracle_quant(w)
+    m = rng.integers(0, M, 4096)
+    n = rng.integers(0, N, 4096)
+    m[:16] = M - 1
+    n[16:32] = N - 1
+    dot, adot = oracle.dot_sampled(ac, asf, wc, wsf, m, n)
+    alpha = float(np.float32(np.float32(ga) * np.float32(gw)))
+    got = f64(host(o1))[m, n]
+    check_close(got, alpha * dot + f64(r)[m, n], alpha * adot, f"{M}x{N}x{K} pair split sampled")

@@ -64,6 +64,12 @@ constexpr uint32_t kRegsEpi = 200;
 static_assert(2 * kRegsSmall + 2 * kRegsEpi == 512, "register split per sub-partition");
 static_assert(kProducers == kEpiWarp0 - 1, "producers: warpgroups 0-1 less the MMA warp");
 constexpr uint16_t kPairMask = 0x3;            // both CTAs of the cluster
+// Shallowest K (stages of 256) for which a partial last wave of tiles is
+// split over all pairs.
+#ifndef NVFP4_PAIR_SPLIT_MIN_STAGES
+#define NVFP4_PAIR_SPLIT_MIN_STAGES 32
+#endif
+constexpr int kPairSplitMinStages = NVFP4_PAIR_SPLIT_MIN_STAGES;
 
 // Instruction descriptor, kind::mxf4nvf4: E2M1 A and B (format 1), UE4M3
 // scales, K-major, N = 256 (bits 17-22 = N/8), M = 256 (bits 24-28 = M/16).
@@ -612,7 +618,8 @@ cudaError_t launch_gemm2(const CUtensorMap& map_a, const CUtensorMap& map_b0, co
     // equal run of the (tile, K stage) units, as the 1-SM kernel's split.
     const int64_t waves = (tiles + all_pairs - 1) / all_pairs;
     const bool split = args.sk_partials != nullptr && args.sk_flags != nullptr && num_sms <= kSplitMaxCtas &&
-                       tiles * stages >= all_pairs && tiles * 10 < waves * all_pairs * 9 && stages >= 32 &&
+                       tiles * stages >= all_pairs && tiles * 10 < waves * all_pairs * 9 &&
+                       stages >= kPairSplitMinStages &&
                        tiles * stages < (int64_t)1 << 31;
     const int64_t pairs = split ? all_pairs : (tiles < all_pairs ? tiles : all_pairs);
     // programmatic launch: the CTAs may start on SMs the previous kernel has

@@ -85,11 +85,16 @@ struct RowShared {
 };
 
 // Float-float sum of squares of this lane's vectors in its warp's share of
-// the row, shuffle-reduced over the warp (fixed order).
+// the row (two independent chains over the even and the odd vectors, then
+// combined), shuffle-reduced over the warp (fixed order).
 __device__ __forceinline__ FF warp_sumsq(const uint4* __restrict__ b, int ng)
 {
-    FF part{0.0f, 0.0f};
-    for (int k = 0; k < ng; k++) part = ff_sumsq8(part, b[k]);
+    FF p0{0.0f, 0.0f}, p1{0.0f, 0.0f};
+    for (int k = 0; k < ng; k += 2) {
+        p0 = ff_sumsq8(p0, b[k]);
+        if (k + 1 < ng) p1 = ff_sumsq8(p1, b[k + 1]);
+    }
+    FF part = ff_add(p0, p1);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
         FF other{__shfl_xor_sync(0xffffffffu, part.hi, o), __shfl_xor_sync(0xffffffffu, part.lo, o)};
@@ -403,6 +408,7 @@ __global__ void __launch_bounds__(kRowThreads, 4)
 {
     griddep_launch_dependents();   // a following GEMM may be scheduled early
     __shared__ RowShared sh;
+    __shared__ uint4 w_sh[NORM ? kResMaxCols / 8 : 1];   // the RMSNorm weight, for both rows
     const int64_t nvec = cols / 8;
     const int64_t kb_pad = cols / 16;
     const int lane = threadIdx.x & 31;
@@ -413,7 +419,6 @@ __global__ void __launch_bounds__(kRowThreads, 4)
     const uint4* w = reinterpret_cast<const uint4*>(norm_w);
     const int64_t ngroups = (nvec + 31) / 32;
     const int ng = ok ? (int)((ngroups - q + kWarpsPerRow - 1) / kWarpsPerRow) : 0;
-    zero_last_scale_tile(sf, rows, kb_pad);
 
     uint4 b[kResGroups];
 #pragma unroll
@@ -421,6 +426,14 @@ __global__ void __launch_bounds__(kRowThreads, 4)
         const int64_t v = (int64_t)(q + k * kWarpsPerRow) * 32 + lane;
         b[k] = (k < ng && v < nvec) ? xr[v] : make_uint4(0, 0, 0, 0);
     }
+    if (NORM) {
+        // the weight goes to shared memory by asynchronous copies, in flight
+        // with the row's loads; the block barrier below makes it visible
+        for (int64_t i = threadIdx.x; i < nvec; i += kRowThreads)
+            asm volatile("cp.async.ca.shared.global [%0], [%1], 16;" ::"r"(smem_u32(&w_sh[i])), "l"(w + i) : "memory");
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    }
+    zero_last_scale_tile(sf, rows, kb_pad);
     float r = 1.0f;
     if (NORM) {
         const FF part = warp_sumsq(b, kResGroups);     // zero padding adds exact zeros
@@ -428,6 +441,7 @@ __global__ void __launch_bounds__(kRowThreads, 4)
             sh.hi[rb][q] = part.hi;
             sh.lo[rb][q] = part.lo;
         }
+        asm volatile("cp.async.wait_all;" ::: "memory");
         __syncthreads();
         if (ok && lane == 0) r = row_inv_rms(sh, rb, cols, eps);
         r = __shfl_sync(0xffffffffu, r, 0);
@@ -442,7 +456,7 @@ __global__ void __launch_bounds__(kRowThreads, 4)
         float f[8];
         unpack8(b[k], f);
         if (NORM) {
-            norm8(f, r, w[v]);
+            norm8(f, r, w_sh[v]);
             b[k] = make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
                               pack_bf16x2(f[6], f[7]));
         }

@@ -139,10 +139,12 @@ def big_weights(nv):
     return w, gpu, orc
 
 
-@pytest.mark.parametrize("T,outliers", [(1, False), (1024, False), (3, True), (777, True)])
+@pytest.mark.parametrize("T,outliers", [(1, False), (1024, False), (3, True), (777, True), (17, True), (128, True),
+                                        (4096, True), (8192, False)])
 def test_mlp_full_size(nv, big_weights, T, outliers):
     """Decode (T=1) and prefill-ubatch (T=1024) MLP at H=5120, I=17408, and
-    the outlier stress (Student-t(3) with 0.1% of channels x100).  STATIC
+    the T sweep with the outlier stress (Student-t(3) with 0.1% of channels
+    x100), up to T=8192 (the SM-pair kernel and its split).  STATIC
     intermediate scale fixed by the oracle on the first rows; outputs
     compared on sampled rows (every row is independent given the scales)."""
     w, gpu, orc = big_weights

@@ -135,21 +135,6 @@ __device__ __forceinline__ void tma_load_1d_pair(uint32_t dst, const CUtensorMap
         : "memory");
 }
 
-// Warm L2 with a tensor tile (no shared-memory destination, no completion).
-__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int32_t x, int32_t y)
-{
-    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
-                     reinterpret_cast<uint64_t>(map)),
-                 "r"(x), "r"(y)
-                 : "memory");
-}
-
-// Warm L2 with a contiguous range (16-B aligned, size % 16 == 0).
-__device__ __forceinline__ void bulk_prefetch(const void* src, uint32_t bytes)
-{
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
-
 // 1-D bulk copy global -> shared (16-B aligned addresses, size % 16 == 0).
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar)
 {

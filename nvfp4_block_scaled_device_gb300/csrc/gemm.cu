@@ -648,8 +648,6 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 
 }  // namespace
 
-size_t gemm_smem_bytes() { return kSmemBytes; }
-
 cudaError_t launch_gemm(const CUtensorMap& map_a, const CUtensorMap& map_b0, const CUtensorMap& map_b1,
                         const GemmArgs& args, int num_sms, cudaStream_t stream)
 {

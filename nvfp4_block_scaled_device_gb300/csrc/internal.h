@@ -131,8 +131,6 @@ cudaError_t launch_gemm2(const CUtensorMap& map_a, const CUtensorMap& map_b0, co
                          const CUtensorMap& map_sfa, const CUtensorMap& map_sfb0, const CUtensorMap& map_sfb1,
                          const GemmArgs& args, int num_sms, cudaStream_t stream);
 
-size_t gemm_smem_bytes();
-
 // Workspace of nvfp4_gemm_swiglu / nvfp4_mlp without the split schedule's
 // partial slots (the least a call accepts; it then runs unsplit).  The
 // public size helpers add the slots for the current device.

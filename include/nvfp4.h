@@ -97,7 +97,7 @@ typedef struct {
 size_t nvfp4_codes_bytes(int64_t rows, int64_t cols);
 /* Bytes of a scale array: pad128(rows) * pad4(cols/16). */
 size_t nvfp4_sf_bytes(int64_t rows, int64_t cols);
-/* Workspace of nvfp4_amax_scale (8 bytes, 256-B aligned). */
+/* Workspace of nvfp4_amax_scale and nvfp4_scale_quantize (256 bytes, 256-B aligned). */
 size_t nvfp4_amax_workspace_bytes(void);
 /* Workspace that lets nvfp4_gemm split its work evenly over all SMs of the
  * current device (8 KB of ready flags + 128 KB per SM; 0 when no device is

@@ -484,7 +484,7 @@ int nvfp4_mlp(const void* x, int64_t T, int64_t H, int64_t ldx, const void* norm
     cudaStream_t st = (cudaStream_t)stream;
 
     uint8_t* ws = static_cast<uint8_t*>(workspace);
-    uint32_t* amax_ws = reinterpret_cast<uint32_t*>(ws);          // words [0,3)
+    uint32_t* amax_ws = reinterpret_cast<uint32_t*>(ws);          // words 0, 1, 32, 48 (g_h: word 16)
     float* g_h = reinterpret_cast<float*>(ws + 64);
     const SplitScratch split = split_scratch(d, ws + 256, ws + base, workspace_bytes - base);
     size_t off = 256 + kSplitFlagBytes;

@@ -20,10 +20,10 @@ constexpr int kRowThreads = 256;
 // several issuing lanes.
 constexpr int kCodeBoxRows = 64;
 
-// Workspace words used by the amax reduction: [0] amax bits, [1] ticket
-// (arrivals at the grid barrier of the fused scale + quantize kernels),
-// [2] departures from that barrier.
-constexpr size_t kAmaxWorkspaceBytes = 16;
+// Workspace words used by the amax reduction: [0] amax bits, [1] ticket;
+// the grid barrier of the fused scale + quantize kernels also counts
+// arrivals at word 32 and departures at word 48 (bytes 128 and 192).
+constexpr size_t kAmaxWorkspaceBytes = 256;
 
 cudaError_t launch_amax_scale(const __nv_bfloat16* x, int64_t rows, int64_t cols, int64_t ldx,
                               const __nv_bfloat16* norm_w, float eps, float* g_out, uint32_t* ws,

@@ -324,8 +324,12 @@ __global__ void finalize_scale_kernel(uint32_t* ws, float* g_out)
 // The global scale needs the amax of the whole matrix before any block can
 // quantize, so the fused kernels run as cooperative launches (every block
 // resident) with one grid-wide barrier between the two phases.  Workspace
-// words: [0] amax bits (atomicMax), [1] arrivals, [2] departures; the last
-// block to depart returns all three to zero.
+// words: [0] amax bits (atomicMax), [kArriveWord] arrivals,
+// [kDepartWord] departures, in separate L2 sectors (the arrival word is
+// polled by every block while the others are updated); the last block to
+// depart returns all three to zero.
+constexpr int kArriveWord = 32;    // byte 128
+constexpr int kDepartWord = 48;    // byte 192
 
 // Block-wide amax of the per-thread values, merged into ws[0]; then the grid
 // barrier; returns the global scale to every thread of the block, or -1 if
@@ -344,12 +348,12 @@ __device__ float grid_global_scale(float amax, uint32_t* ws, float* g_out, int* 
         // non-negative binary32 values order like their bit patterns
         atomicMax(&ws[0], __float_as_uint(amax));
         __threadfence();
-        atomicAdd(&ws[1], 1u);
+        atomicAdd(&ws[kArriveWord], 1u);
         const uint64_t t0 = clock64();
         float g = -1.0f;
         for (;;) {
             uint32_t arrived;
-            asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(arrived) : "l"(ws + 1) : "memory");
+            asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(arrived) : "l"(ws + kArriveWord) : "memory");
             if (arrived >= gridDim.x) {
                 uint32_t bits;
                 asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(bits) : "l"(ws) : "memory");
@@ -367,10 +371,10 @@ __device__ float grid_global_scale(float amax, uint32_t* ws, float* g_out, int* 
             // every block has read the amax before it departs: the last one
             // to depart clears the words for the next call
             __threadfence();
-            if (atomicAdd(&ws[2], 1u) == gridDim.x - 1) {
+            if (atomicAdd(&ws[kDepartWord], 1u) == gridDim.x - 1) {
                 atomicExch(&ws[0], 0u);
-                atomicExch(&ws[1], 0u);
-                atomicExch(&ws[2], 0u);
+                atomicExch(&ws[kArriveWord], 0u);
+                atomicExch(&ws[kDepartWord], 0u);
             }
         }
         s_g = g;

@@ -47,7 +47,7 @@ def test_size_helpers(L):
     assert nv.sf_bytes(128, 64) == 128 * 4
     assert nv.sf_bytes(129, 5120) == 256 * 320
     assert nv.sf_bytes(1, 17408) == 128 * 1088
-    assert nv.amax_workspace_bytes() >= 8
+    assert nv.amax_workspace_bytes() >= 256
     assert nv.gemm_workspace_bytes() >= 8192            # ready flags (+ partial slots with a device)
     assert nv.swiglu_workspace_bytes(1024, 17408, nv.NVFP4_INTER_DYNAMIC) >= 1024 * 17408 * 2
     assert nv.mlp_workspace_bytes(1024, 5120, 17408, nv.NVFP4_INTER_STATIC) >= (

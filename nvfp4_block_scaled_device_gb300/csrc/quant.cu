@@ -111,17 +111,26 @@ __device__ __forceinline__ FF warp_sumsq(const uint4* __restrict__ b, int ng)
 // exact remainder hi - q n by a fused multiply-add, and the correction
 // (remainder + lo) / n added to q.  The result is the correctly rounded
 // quotient except within about 2^-24 of an ulp of a tie -- the same margin at
-// which the float-float sum itself may differ from the exact sum.
-__device__ __forceinline__ float row_inv_rms(const RowShared& sh, int rb, int64_t cols, float eps)
+// which the float-float sum itself may differ from the exact sum.  Both
+// divisions by n are correctly rounded quotients formed from rcp_n = RN(1/n)
+// (div_by_recip; a full division where the quotient would be subnormal), and
+// 1/sqrt is the correctly rounded reciprocal of the correctly rounded root.
+__device__ __forceinline__ float div_by_n(float a, float n, float rcp_n)
+{
+    const float q = div_by_recip(a, n, rcp_n);
+    return fabsf(q) < 1.17549435e-38f ? __fdiv_rn(a, n) : q;
+}
+
+__device__ __forceinline__ float row_inv_rms(const RowShared& sh, int rb, int64_t cols, float rcp_n, float eps)
 {
     FF t{sh.hi[rb][0], sh.lo[rb][0]};
 #pragma unroll
     for (int q = 1; q < kWarpsPerRow; q++) t = ff_add(t, FF{sh.hi[rb][q], sh.lo[rb][q]});
     const float n = (float)cols;                        // exact: cols < 2^24
-    const float q0 = __fdiv_rn(t.hi, n);
+    const float q0 = div_by_n(t.hi, n, rcp_n);
     const float rem = __fmaf_rn(-q0, n, t.hi);          // exact
-    const float ms = __fadd_rn(q0, __fdiv_rn(__fadd_rn(rem, t.lo), n));
-    return __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, eps)));
+    const float ms = __fadd_rn(q0, div_by_n(__fadd_rn(rem, t.lo), n, rcp_n));
+    return __frcp_rn(__fsqrt_rn(__fadd_rn(ms, eps)));
 }
 
 // One 8-element vector v of a row, already in f (normalised when NORM):
@@ -194,7 +203,7 @@ __device__ __forceinline__ void row_share(const uint4* __restrict__ xr, int64_t 
             }
             __syncthreads();
             // one lane per warp (binary64 is slow on this GPU), then broadcast
-            if (row_valid && lane == 0) r = row_inv_rms(sh, rb, cols, eps);
+            if (row_valid && lane == 0) r = row_inv_rms(sh, rb, cols, __frcp_rn((float)cols), eps);
             r = __shfl_sync(0xffffffffu, r, 0);
             __syncthreads();                            // sh is reused by the block's next rows
         }
@@ -228,7 +237,7 @@ __device__ __forceinline__ void row_share(const uint4* __restrict__ xr, int64_t 
             sh.lo[rb][q] = part.lo;
         }
         __syncthreads();
-        if (lane == 0) r = row_inv_rms(sh, rb, cols, eps);
+        if (lane == 0) r = row_inv_rms(sh, rb, cols, __frcp_rn((float)cols), eps);
         r = __shfl_sync(0xffffffffu, r, 0);
         __syncthreads();
     }
@@ -440,6 +449,7 @@ __global__ void __launch_bounds__(kRowThreads, 4)
     zero_last_scale_tile(sf, rows, kb_pad);
     float r = 1.0f;
     if (NORM) {
+        const float rcp_n = __frcp_rn((float)cols);    // off the row's critical path
         const FF part = warp_sumsq(b, kResGroups);     // zero padding adds exact zeros
         if (lane == 0) {
             sh.hi[rb][q] = part.hi;
@@ -447,7 +457,7 @@ __global__ void __launch_bounds__(kRowThreads, 4)
         }
         asm volatile("cp.async.wait_all;" ::: "memory");
         __syncthreads();
-        if (ok && lane == 0) r = row_inv_rms(sh, rb, cols, eps);
+        if (ok && lane == 0) r = row_inv_rms(sh, rb, cols, rcp_n, eps);
         r = __shfl_sync(0xffffffffu, r, 0);
     }
     // phase 1: the row (normalised when NORM, kept as bf16) and its amax

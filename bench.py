@@ -263,6 +263,23 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------ multi-rank timing
+def slowest_rank_ms(ms, dist=None, device=None):
+    """Duration of the timed region as the whole job sees it: the maximum over
+    the ranks (all-reduce MAX), or the local value in a single process."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return ms
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(world, units_per_rank, ms):
+    """Units per second over all ranks (weak scaling: every rank processed
+    units_per_rank within the slowest rank's time)."""
+    return world * units_per_rank / (ms / 1e3)
+
+
 # ----------------------------------------------------------- GPU (ours)
 def run_ours(args):
     import __graft_entry__
@@ -374,13 +391,9 @@ def run_ours(args):
     if dist:
         dist.barrier()
     clk = clocks.stop()
-    ms_total = e0.elapsed_time(e1)
-    if dist:
-        t = torch.tensor([ms_total], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = t.item()
+    ms_total = slowest_rank_ms(e0.elapsed_time(e1), dist, dev)
     ms_step = ms_total / args.steps
-    value = world * T * args.steps / (ms_total / 1e3)
+    value = whole_job_rate(world, T * args.steps, ms_total)
 
     # per-GEMM times from the last replay's evented steps
     gemm = {}
@@ -413,12 +426,8 @@ def run_ours(args):
     pipe.join()
     s1.record(stream)
     torch.cuda.synchronize()
-    ms_e2e = s0.elapsed_time(s1)
-    if dist:
-        t = torch.tensor([ms_e2e], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_e2e = t.item()
-    e2e = {"value": world * T * ke / (ms_e2e / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": x.numel() * 2,
+    ms_e2e = slowest_rank_ms(s0.elapsed_time(s1), dist, dev)
+    e2e = {"value": whole_job_rate(world, T * ke, ms_e2e), "unit": "tokens/s", "h2d_bytes_per_step": x.numel() * 2,
            "d2h_bytes_per_step": out.numel() * 2, "steps": ke,
            "copies": "pinned host <-> device every step, overlapped with the neighbouring steps' compute"}
 

@@ -23,6 +23,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libnvfp4.so")
 
 NVFP4_OK = 0
+NVFP4_ERR_TIMEOUT = 6        # device-side: a bounded wait ran out (status word: 6 * 100 + site)
 NVFP4_INTER_STATIC = 0
 NVFP4_INTER_DYNAMIC = 1
 

@@ -280,6 +280,71 @@ def whole_job_rate(world, units_per_rank, ms):
     return world * units_per_rank / (ms / 1e3)
 
 
+# ------------------------------------------------- side measurements
+def side_measurements(nv, W, stream, hbm_gbs, fp4_peak):
+    """After the timed region, outside the metric: the one-launch scale +
+    quantize at R=16384 x K=5120 (168 MB of bf16 per pass; achieved GB/s on
+    the algorithmic bytes 2RK read + 0.5625RK written) and every GEMM shape of
+    the block at T=1 (decode) and T=16384 (long prefill), with the block's
+    weights, each timed over a few launches with CUDA events."""
+    def timed(fn, iters):
+        with torch.cuda.stream(stream):
+            fn()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(iters):
+                fn()
+            e1.record(stream)
+        stream.synchronize()
+        return e0.elapsed_time(e1) / iters * 1e3      # us
+
+    dev = W["o"].codes.device
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(7)
+    out = {}
+    R, K = 16384, H
+    x = torch.randn((R, K), generator=gen, device=dev).bfloat16()
+    w = (1 + 0.05 * torch.randn((K,), generator=gen, device=dev)).bfloat16()
+    t = nv.NVFP4Tensor.empty(R, K, dev)
+    ws = nv.workspace(256, dev)
+    alg = 2 * R * K + 0.5625 * R * K
+    for name, nw in (("scale_quantize_R16384", None), ("norm_scale_quantize_R16384", w)):
+        us = timed(lambda: nv.nvfp4_scale_quantize(x, t, ws, nw, 1e-6, stream), 10)
+        out[name] = {"us": us, "GB/s": alg / us / 1e3, "frac_of_hbm": alg / us / 1e3 / hbm_gbs}
+    del x, t
+    gws = nv.workspace(nv.gemm_workspace_bytes(), dev)
+    for T in (1, 16384):
+        A = {Kk: nv.NVFP4Tensor.empty(T, Kk, dev) for Kk in (H, I)}
+        for Kk, a in A.items():
+            nv.nvfp4_scale_quantize(torch.randn((T, Kk), generator=gen, device=dev).bfloat16(), a, ws, None, 1e-6,
+                                    stream)
+        res = {}
+        for name, Wt, Kk in (("qkv", W["qkv"], H), ("o", W["o"], H), ("down", W["down"], I)):
+            o = torch.empty((T, Wt.rows), dtype=torch.bfloat16, device=dev)
+            us = timed(lambda: nv.nvfp4_gemm(A[Kk], Wt, o, None, stream, gws), 5)
+            res[name] = {"us": us, "TFLOP/s": 2 * T * Wt.rows * Kk / us / 1e6}
+        s_t = nv.NVFP4Tensor.empty(T, I, dev)
+        g_i = torch.tensor([0.01], dtype=torch.float32, device=dev)
+        sws = nv.workspace(nv.swiglu_workspace_bytes(T, I, nv.NVFP4_INTER_STATIC), dev)
+        us = timed(lambda: nv.nvfp4_gemm_swiglu(A[H], W["gate"], W["up"], nv.NVFP4_INTER_STATIC, g_i, s_t, sws,
+                                                None, stream), 5)
+        res["gate_up_swiglu"] = {"us": us, "TFLOP/s": 2 * T * 2 * I * H / us / 1e6}
+        for v in res.values():
+            v["frac_of_fp4_peak"] = v["TFLOP/s"] / fp4_peak
+        if T == 1:
+            wbytes = sum(Wt.codes.numel() + Wt.sf.numel() for Wt in W.values())
+            for name in res:
+                Wt = {"qkv": [W["qkv"]], "o": [W["o"]], "down": [W["down"]],
+                      "gate_up_swiglu": [W["gate"], W["up"]]}[name]
+                b = sum(x_.codes.numel() + x_.sf.numel() for x_ in Wt)
+                res[name]["weight_GB/s"] = b / res[name]["us"] / 1e3
+            res["weights_MB"] = wbytes / 1e6
+        out[f"gemm_T{T}"] = res
+        del A
+    assert nv.device_status() == 0
+    return out
+
+
 # ----------------------------------------------------------- GPU (ours)
 def run_ours(args):
     import __graft_entry__
@@ -435,6 +500,8 @@ def run_ours(args):
         if dist:
             dist.destroy_process_group()
         return
+    hbm_gbs, _, bf16_sust_peak, _ = peaks()
+    side = side_measurements(nv, W, stream, hbm_gbs, bf16_sust_peak * FP4_PER_BF16) if args.side else None
 
     hbm, bf16_burst, bf16_sust, src = peaks()
     fp4_peak = bf16_sust * FP4_PER_BF16
@@ -471,6 +538,7 @@ def run_ours(args):
         "fp4_peak_tflops": fp4_peak,
         "roofline": roofline,
         "e2e": e2e,
+        "side": side,
         "clocks": clk,
     }
     if world == 1 and not args.no_cpu_baseline:
@@ -488,6 +556,8 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--T", type=int, default=T_DEFAULT)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-side", dest="side", action="store_false",
+                    help="skip the side measurements (quantize at R=16384, GEMMs at T=1 and T=16384)")
     ap.add_argument("--only", choices=("swiglu", "down", "qkv", "norm_quantize", "step"),
                     help="profiling target: run one kernel of the step --only-reps times and exit")
     ap.add_argument("--only-reps", type=int, default=3)

@@ -1,10 +1,11 @@
 // Row kernels of the NVFP4 path: the device global scale (amax reduction,
 // optionally of the RMSNorm of the rows) and the bf16 -> NVFP4 quantizer
-// (optionally fused with that RMSNorm).  Four warps per row (two rows per
-// 256-thread block, at least three blocks per SM), 16-byte vector loads, a
-// row share of up to 1536 columns per warp held in registers, shuffle
-// reductions; both kernels share one row routine so the RMSNorm they
-// compute is bit-identical.
+// (optionally fused with that RMSNorm), as two kernels and as one
+// cooperative launch with a grid barrier between them (the path's form).
+// Four warps per row (two rows per 256-thread block, three or four blocks per
+// SM), 16-byte vector loads, a row share of up to 1536 columns per warp held
+// in registers, shuffle reductions; all kernels compute the RMSNorm with the
+// same routines, so it is bit-identical among them.
 //
 // Sources: "PERFORMANCE -- verified hot-path audit and prioritized fixes"
 // P0 (scale = max(amax, 1e-8) / (6 * 448), computed on the device, handed on

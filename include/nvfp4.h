@@ -26,6 +26,12 @@
  *  - Every pointer argument is a DEVICE pointer unless stated otherwise, owned
  *    by the caller.  No function allocates, frees or synchronises; all work is
  *    enqueued on `stream` (a cudaStream_t; NULL is the legacy default stream).
+ *  - The GEMM kernels use programmatic dependent launch: they may start
+ *    while the previous kernel of the stream still runs, and read their
+ *    operands only after it has completed -- except inside nvfp4_mlp, whose
+ *    GEMMs fetch the weights early (the weights were complete before the
+ *    call's first, plainly launched kernel started): a tensor quantized by
+ *    the launch just before a GEMM call is safe to use as its weight.
  *  - The return value is a status (NVFP4_OK = 0).  Argument errors are
  *    detected on the host before anything is enqueued.  NVFP4_ERR_CUDA
  *    reports a launch error (cudaGetLastError); asynchronous failures show

@@ -180,7 +180,7 @@ SplitScratch split_scratch(const DeviceInfo* d, uint8_t* flags, uint8_t* partial
 int run_swiglu(const DeviceInfo* d, const nvfp4_tensor_t* A, const nvfp4_tensor_t* Wg, const nvfp4_tensor_t* Wu,
                int mode, float* g_inter, uint8_t* s_codes, int64_t ld_s_codes, uint8_t* s_sf,
                __nv_bfloat16* s_bf16_user, uint32_t* amax_ws, __nv_bfloat16* s_bf16_scratch, SplitScratch split,
-               cudaStream_t stream)
+               bool weights_early, cudaStream_t stream)
 {
     const int64_t T = A->rows, I = Wg->rows;
     CUtensorMap ma, mg, mu;
@@ -200,6 +200,7 @@ int run_swiglu(const DeviceInfo* d, const nvfp4_tensor_t* A, const nvfp4_tensor_
     a.gb0 = Wg->g;
     a.gb1 = Wu->g;
     a.status = d->status;
+    a.weights_early = weights_early ? 1 : 0;
     a.s_codes = s_codes;
     a.ld_s_codes = ld_s_codes;
     a.s_sf = s_sf;
@@ -453,7 +454,8 @@ int nvfp4_gemm_swiglu(const nvfp4_tensor_t* A, const nvfp4_tensor_t* W_gate, con
     return run_swiglu(d, A, W_gate, W_up, inter_mode, g_inter, s_codes, ld_s_codes, s_sf,
                       static_cast<__nv_bfloat16*>(s_bf16), reinterpret_cast<uint32_t*>(ws),
                       reinterpret_cast<__nv_bfloat16*>(ws + 256 + kSplitFlagBytes),
-                      split_scratch(d, ws + 256, ws + base, workspace_bytes - base), (cudaStream_t)stream);
+                      split_scratch(d, ws + 256, ws + base, workspace_bytes - base), false,
+                      (cudaStream_t)stream);
 }
 
 int nvfp4_mlp(const void* x, int64_t T, int64_t H, int64_t ldx, const void* norm_w, float eps,
@@ -507,8 +509,11 @@ int nvfp4_mlp(const void* x, int64_t T, int64_t H, int64_t ldx, const void* norm
     const nvfp4_tensor_t h = {h_codes, h_sf, g_h, T, H, H / 2};
     // the gate/up kernel and the down kernel run one after the other on the
     // stream, so they share the split scratch
+    // the weights were complete before the call's first launch (the plain
+    // launch of step 1 waits for all earlier work), and no launch of the call
+    // writes them: the GEMMs may fetch them early
     NVFP4_TRY(run_swiglu(d, &h, W_gate, W_up, inter_mode, g_inter, s_codes, I / 2, s_sf, nullptr, amax_ws,
-                         s_bf16_scratch, split, st));
+                         s_bf16_scratch, split, true, st));
     // 4: down GEMM (+ residual)
     const nvfp4_tensor_t s = {s_codes, s_sf, g_inter, T, I, I / 2};
     CUtensorMap ma, mb;
@@ -532,6 +537,7 @@ int nvfp4_mlp(const void* x, int64_t T, int64_t H, int64_t ldx, const void* norm
     a.status = d->status;
     a.sk_flags = split.flags;
     a.sk_partials = split.partials;
+    a.weights_early = 1;
     NVFP4_CUDA(run_gemm(ma, mb, mb, a, d, st));
     return NVFP4_OK;
 }

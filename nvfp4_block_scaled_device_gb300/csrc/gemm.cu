@@ -293,10 +293,11 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             // stale shared memory only feeds accumulator rows >= M or columns
             // >= N, never stored.
             const int p = warp < kMmaWarp ? warp : warp - 1;
-            // The weight boxes (producers 2-5) do not depend on the previous
-            // kernel and start at once; A and the scale tiles (producers 0,
-            // 1, 6) wait for it to complete (programmatic launch).
-            if (p < 2 || p == 6) griddep_wait();
+            // A and the scale tiles (producers 0, 1, 6) wait for the previous
+            // kernel to complete (programmatic launch); the weight boxes
+            // (producers 2-5) start at once when the caller vouches that the
+            // weights were complete before that kernel started.
+            if (p < 2 || p == 6 || !args.weights_early) griddep_wait();
             const uint32_t full0 = smem_u32(&ctrl->full[0]);
             const uint32_t empty0 = smem_u32(&ctrl->empty[0]);
             constexpr uint32_t kBox = kCodeBoxRows * 128u;
@@ -684,7 +685,7 @@ cudaError_t launch_gemm(const CUtensorMap& map_a, const CUtensorMap& map_b0, con
                        tiles * stages >= num_sms && tiles * 10 < waves * num_sms * 9 && stages >= 32 &&
                        tiles * stages < (int64_t)1 << 31;
     // programmatic launch: the CTAs may start on SMs the previous kernel has
-    // left and fetch weights before it completes
+    // left, and fetch weights before it completes when args.weights_early
     if (split)
         return launch_programmatic(gemm_kernel<true>, dim3((unsigned)num_sms), dim3(kNumThreads), kSmemBytes, stream,
                                    map_a, map_b0, map_b1, args);

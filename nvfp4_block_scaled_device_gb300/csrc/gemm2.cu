@@ -288,10 +288,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
             // stages or of the next rows (or zero fill past the end), which no
             // MMA reads.
             const int p = warp < kMmaWarp ? warp : warp - 1;
-            // The weight boxes and scales (producers 2, 3, 5, 6) do not
-            // depend on the previous kernel and start at once; A and its
-            // scales (producers 0, 1, 4) wait for it to complete.
-            if (p < 2 || p == 4) griddep_wait();
+            // A and its scales (producers 0, 1, 4) wait for the previous
+            // kernel to complete; the weight boxes and scales (producers 2,
+            // 3, 5, 6) start at once when the caller vouches that the weights
+            // were complete before that kernel started.
+            if (p < 2 || p == 4 || !args.weights_early) griddep_wait();
             const uint32_t full_leader0 = map_to_cta(smem_u32(&ctrl->full[0]), 0);
             const uint32_t empty0 = smem_u32(&ctrl->empty[0]);
             constexpr uint32_t kBox = kCodeBoxRows * 128u;
@@ -623,7 +624,7 @@ cudaError_t launch_gemm2(const CUtensorMap& map_a, const CUtensorMap& map_b0, co
                        tiles * stages < (int64_t)1 << 31;
     const int64_t pairs = split ? all_pairs : (tiles < all_pairs ? tiles : all_pairs);
     // programmatic launch: the CTAs may start on SMs the previous kernel has
-    // left and fetch weights before it completes
+    // left, and fetch weights before it completes when args.weights_early
     if (split)
         return launch_programmatic(gemm2_kernel<true>, dim3((unsigned)(2 * pairs)), dim3(kNumThreads), kSmemBytes,
                                    stream, map_a, map_b0, map_b1, map_sfa, map_sfb0, map_sfb1, args);

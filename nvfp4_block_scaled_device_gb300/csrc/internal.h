@@ -107,6 +107,11 @@ struct GemmArgs {
     // kSplitSlotFloats per CTA) and per-warp ready flags.
     float* sk_partials;
     int* sk_flags;
+    // nonzero: the weight operands (B0/B1 codes and scales) were complete
+    // before the previous kernel of the stream started, so their loads may
+    // run ahead of griddep_wait(); zero: every load waits for that kernel
+    // (which may be the one that wrote them) to complete
+    int weights_early;
 };
 
 // Split-schedule workspace: a fixed block of ready flags (one per epilogue

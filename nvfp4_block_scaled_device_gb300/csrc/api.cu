@@ -6,6 +6,7 @@
 
 #include <mutex>
 
+#include "gemv.h"
 #include "internal.h"
 #include "nvfp4.h"
 
@@ -142,8 +143,10 @@ constexpr int64_t kPairMinRows = 129;
 #endif
 
 cudaError_t run_gemm(const CUtensorMap& ma, const CUtensorMap& mb0, const CUtensorMap& mb1, const GemmArgs& a,
-                     const DeviceInfo* d, cudaStream_t stream)
+                     const DecodeOperands& ops, const DeviceInfo* d, cudaStream_t stream)
 {
+    // one or two activation rows: a weight stream, on the CUDA cores
+    if (gemv_eligible(a, d->num_sms)) return launch_gemv(ops, a, d->num_sms, stream);
     const bool swiglu = a.epilogue != kEpiBf16;
     const int64_t pair_tiles = (a.M + 255) / 256 * (swiglu ? a.N / 128 : (a.N + 255) / 256);
     if (a.M >= kPairMinRows && pair_tiles * 2 >= d->num_sms) {
@@ -187,6 +190,7 @@ int run_swiglu(const DeviceInfo* d, const nvfp4_tensor_t* A, const nvfp4_tensor_
     NVFP4_TRY(make_codes_map(&ma, A->codes, T, A->cols / 2, A->ld));
     NVFP4_TRY(make_codes_map(&mg, Wg->codes, I, Wg->cols / 2, Wg->ld));
     NVFP4_TRY(make_codes_map(&mu, Wu->codes, I, Wu->cols / 2, Wu->ld));
+    const DecodeOperands ops = {A->codes, A->ld, Wg->codes, Wg->ld, Wu->codes, Wu->ld};
     GemmArgs a = {};
     a.M = T;
     a.N = I;
@@ -212,14 +216,14 @@ int run_swiglu(const DeviceInfo* d, const nvfp4_tensor_t* A, const nvfp4_tensor_
         a.g_inter = g_inter;
         a.s_bf16 = s_bf16_user;
         a.ld_s = I;
-        NVFP4_CUDA(run_gemm(ma, mg, mu, a, d, stream));
+        NVFP4_CUDA(run_gemm(ma, mg, mu, a, ops, d, stream));
     } else {
         __nv_bfloat16* s_bf16 = s_bf16_user ? s_bf16_user : s_bf16_scratch;
         a.epilogue = kEpiSwigluBf16;
         a.s_bf16 = s_bf16;
         a.ld_s = I;
         a.amax_ws = amax_ws;
-        NVFP4_CUDA(run_gemm(ma, mg, mu, a, d, stream));
+        NVFP4_CUDA(run_gemm(ma, mg, mu, a, ops, d, stream));
         NVFP4_CUDA(launch_finalize_scale(amax_ws, g_inter, stream));
         NVFP4_CUDA(launch_quantize(s_bf16, T, I, I, nullptr, 0.0f, g_inter, s_codes, ld_s_codes, s_sf, nullptr,
                                    d->num_sms, stream));
@@ -431,7 +435,8 @@ int nvfp4_gemm(const nvfp4_tensor_t* A, const nvfp4_tensor_t* W, void* out, int6
         a.sk_flags = sp.flags;
         a.sk_partials = sp.partials;
     }
-    NVFP4_CUDA(run_gemm(ma, mb, mb, a, d, (cudaStream_t)stream));
+    const DecodeOperands ops = {A->codes, A->ld, W->codes, W->ld, W->codes, W->ld};
+    NVFP4_CUDA(run_gemm(ma, mb, mb, a, ops, d, (cudaStream_t)stream));
     return NVFP4_OK;
 }
 
@@ -538,7 +543,8 @@ int nvfp4_mlp(const void* x, int64_t T, int64_t H, int64_t ldx, const void* norm
     a.sk_flags = split.flags;
     a.sk_partials = split.partials;
     a.weights_early = 1;
-    NVFP4_CUDA(run_gemm(ma, mb, mb, a, d, st));
+    const DecodeOperands ops = {s.codes, I / 2, W_down->codes, W_down->ld, W_down->codes, W_down->ld};
+    NVFP4_CUDA(run_gemm(ma, mb, mb, a, ops, d, st));
     return NVFP4_OK;
 }
 

@@ -143,8 +143,9 @@ def test_full_size_sampled(nv, ws, M, N, K, split):
 # idle (so the split is taken), including a ragged M, a K with a partial
 # last stage (K = 8384: 32 full stages of 256 + 192), and tiles with only a
 # few valid rows (M = 1, 3, 131) whose partials are fetched column-wise, one
-# of them combining some 40 partials per tile.
-@pytest.mark.parametrize("M,N,K", [(777, 512, 8192), (300, 1024, 8192), (300, 768, 8384), (1, 5120, 8192),
+# of them combining some 40 partials per tile.  (M = 1 with weights above
+# 32 MiB: smaller ones go to the decode kernel.)
+@pytest.mark.parametrize("M,N,K", [(777, 512, 8192), (300, 1024, 8192), (300, 768, 8384), (1, 5120, 16384),
                                    (3, 1024, 16384), (131, 1024, 8192)])
 def test_split_schedule(nv, ws, M, N, K):
     got, ref, absref = run_case(nv, ws, M, N, K, seed=M + 7 * N + K, split=True)

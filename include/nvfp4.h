@@ -206,6 +206,11 @@ int nvfp4_scale_quantize(const void* x, int64_t rows, int64_t cols, int64_t ldx,
  *            the GEMM may split its tiles' K ranges over all SMs when whole
  *            tiles would leave part of the GPU idle (fp32 partials combined
  *            in the workspace); otherwise whole tiles are spread over the SMs.
+ * With M <= 2 and at most 32 MiB of weight codes the GEMM runs instead as a
+ * weight stream on the CUDA cores (exact int32 sums of E2M1 code products
+ * per 16-element block, block scales applied exactly in fp32, fp32
+ * accumulation): the same result up to the fp32 summation order; the
+ * workspace is not used.  nvfp4_gemm_swiglu and nvfp4_mlp do the same.
  * Requires K == A->cols == W->cols, K % 64 == 0, N % 16 == 0.
  */
 int nvfp4_gemm(const nvfp4_tensor_t* A, const nvfp4_tensor_t* W,

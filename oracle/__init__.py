@@ -83,6 +83,7 @@ def lib():
                 "oracle_rmsnorm": (None, [vp, i64, i64, i64, vp, f32, vp, i64]),
                 "oracle_swiglu1": (ctypes.c_uint16, [ctypes.c_uint16, ctypes.c_uint16]),
                 "oracle_swiglu": (None, [vp, vp, i64, vp]),
+                "oracle_rope": (None, [vp, i64, i64, i64, vp, vp, vp, i64, i64, i64, i64, i64, i32, vp, i64]),
                 "oracle_mlp": (None, [vp, i64, i64, i64, i64, vp, f32,
                                       vp, vp, f32, vp, vp, f32, vp, vp, f32,
                                       f32, i32, vp, i64,
@@ -242,6 +243,25 @@ def swiglu(gate_bits, up_bits):
     s = np.empty_like(g)
     lib().oracle_swiglu(_p(g), _p(u), g.size, _p(s))
     return s
+
+
+def rope(y_bits, pos, cos_t, sin_t, col0, heads, head_dim, rope_dim, inverse=False):
+    """Rotary embedding of bf16 rows y [rows, cols] (see oracle_rope): the
+    `heads` heads of head_dim columns from column col0 get their last
+    rope_dim columns rotated as (even, odd) pairs by the angles of table row
+    pos[t] (cos_t, sin_t: float32 [positions, >= rope_dim/2])."""
+    y = _c(y_bits, np.uint16)
+    p = _c(pos, np.int32)
+    ct = _c(cos_t, np.float32)
+    st = _c(sin_t, np.float32)
+    rows, cols = y.shape
+    assert p.shape == (rows,) and ct.shape == st.shape and ct.shape[1] * 2 >= rope_dim
+    assert rope_dim % 2 == 0 and 0 < rope_dim <= head_dim and col0 + heads * head_dim <= cols
+    assert p.min() >= 0 and p.max() < ct.shape[0]
+    out = np.empty_like(y)
+    lib().oracle_rope(_p(y), rows, cols, cols, _p(p), _p(ct), _p(st), ct.shape[1], col0, heads, head_dim, rope_dim,
+                      int(bool(inverse)), _p(out), cols)
+    return out
 
 
 def mlp(x_bits, norm_w_bits, wg, wu, wd, g_inter=None, add_residual=True, eps=1e-6):

@@ -32,6 +32,10 @@
  *  [SFL] the 128-row x 4-column scale-factor tile layout that the Blackwell
  *        block-scaled MMA reads (public PTX ISA / cuBLAS "block scaling
  *        factors layout").
+ *  [ROPE] "PERFORMANCE -- verified hot-path audit and prioritized fixes",
+ *        section P5 (RoPE on the last rope_dim columns of each head, as
+ *        (even, odd) pairs, in float32 from bf16 and back) and the list of
+ *        structural targets, item 3 (RoPE fused into the Q/KV GEMM epilogue).
  *
  * Readings taken where the sources are silent are stated at each function.
  */
@@ -418,6 +422,46 @@ uint16_t oracle_swiglu1(uint16_t gate, uint16_t up)
 void oracle_swiglu(const uint16_t* gate, const uint16_t* up, int64_t n, uint16_t* s)
 {
     for (int64_t i = 0; i < n; i++) s[i] = oracle_swiglu1(gate[i], up[i]);
+}
+
+/* ------------------------------------------------------------------ */
+/* Rotary position embedding of projection output rows [ROPE]         */
+/* ------------------------------------------------------------------ */
+
+/* y: bf16 [rows x cols] (pitch ldy), e.g. the QKV GEMM output.  The `heads`
+ * heads of head_dim columns starting at column col0 are rotated; every other
+ * column is copied.  In a rotated head the first head_dim - rope_dim columns
+ * are copied and the last rope_dim form rope_dim/2 pairs (e, o) = (x[2i],
+ * x[2i+1]); with c = cos_t[pos[t]][i], s = sin_t[pos[t]][i] (tables of pitch
+ * table_ld floats):
+ *   forward: e' = e*c - o*s,  o' = e*s + o*c
+ *   inverse: e' = e*c + o*s,  o' = o*c - e*s
+ * each product, sum and difference one binary32 operation, e' and o' then
+ * rounded to bf16 (RNE).
+ * Reading: the tables are inputs (the page indexes cos and sin by position
+ * and does not say how they are built). */
+void oracle_rope(const uint16_t* y, int64_t rows, int64_t cols, int64_t ldy, const int32_t* pos,
+                 const float* cos_t, const float* sin_t, int64_t table_ld, int64_t col0, int64_t heads,
+                 int64_t head_dim, int64_t rope_dim, int inverse, uint16_t* out, int64_t ldo)
+{
+    for (int64_t t = 0; t < rows; t++) {
+        for (int64_t c = 0; c < cols; c++) out[t * ldo + c] = y[t * ldy + c];
+        const float* ct = cos_t + (int64_t)pos[t] * table_ld;
+        const float* st = sin_t + (int64_t)pos[t] * table_ld;
+        for (int64_t h = 0; h < heads; h++) {
+            const int64_t base = col0 + h * head_dim + (head_dim - rope_dim);
+            for (int64_t i = 0; i < rope_dim / 2; i++) {
+                const float e = (float)oracle_bf16_value(y[t * ldy + base + 2 * i]);
+                const float o = (float)oracle_bf16_value(y[t * ldy + base + 2 * i + 1]);
+                const float c = ct[i], s = st[i];
+                const float ec = e * c, os = o * s, es = e * s, oc = o * c;
+                const float e2 = inverse ? ec + os : ec - os;
+                const float o2 = inverse ? oc - es : es + oc;
+                out[t * ldo + base + 2 * i] = oracle_bf16_from_double((double)e2);
+                out[t * ldo + base + 2 * i + 1] = oracle_bf16_from_double((double)o2);
+            }
+        }
+    }
 }
 
 /* ------------------------------------------------------------------ */

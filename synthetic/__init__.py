@@ -1,8 +1,9 @@
 """Seeded synthetic inputs shared by the tests, the benchmark and the oracle.
 
 This module only draws random numbers and rounds them to bf16 (the input
-format); it holds none of the NVFP4 arithmetic (no scales, no quantization,
-no GEMM).  Every generator is numpy PCG64 (``default_rng(seed)``) drawing
+format), and builds the rotary cos/sin tables that the rotary embedding
+takes as inputs; it holds none of the NVFP4 arithmetic (no scales, no
+quantization, no GEMM) and none of the rotation itself.  Every generator is numpy PCG64 (``default_rng(seed)``) drawing
 float32, rounded to bf16 with round-to-nearest-even by torch's CPU cast.
 bf16 tensors are returned as numpy ``uint16`` bit patterns.
 
@@ -108,3 +109,12 @@ def activations(T: int, seed: int, h=H, outliers=False) -> np.ndarray:
     if outliers:
         return student_t_outliers(rng, (T, h))
     return normal(rng, (T, h))
+
+
+def rope_tables(positions: int, rope_dim: int, theta: float = 10000.0):
+    """cos and sin tables, float32 [positions, rope_dim/2], of the usual
+    rotary angles p * theta^(-2i/rope_dim) (computed in float64, rounded
+    once): inputs of the rotary embedding, not part of the NVFP4 path."""
+    i = np.arange(rope_dim // 2, dtype=np.float64)
+    ang = np.arange(positions, dtype=np.float64)[:, None] * theta ** (-2.0 * i / rope_dim)[None, :]
+    return np.cos(ang).astype(np.float32), np.sin(ang).astype(np.float32)

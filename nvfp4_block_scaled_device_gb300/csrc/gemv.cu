@@ -17,10 +17,11 @@
 //   - that sum times the two E4M3 block scales is exact in fp32, and the
 //     blocks accumulate in fp32 (the same arithmetic as the tensor pipe's
 //     block-scaled MMA, in another summation order).
-// Sources: "CUDA: NVFP4 prefill on Blackwell leaves ~1.45x performance on
-// the table" (llama.cpp discussion 28514) on decode (T=1) running the same
-// FP4 weights through a separate path, and "PERFORMANCE -- verified hot-path
-// audit" E9 (single-token step).
+// Sources: "tp>1 prefill is host-bound: per-token fp4 GEMM + per-layer H2D
+// activation staging" (vllm.cpp issue 2144), whose profile compares the fp4
+// MLP of a decode step (T=1) with T=5; "PERFORMANCE -- verified hot-path
+// audit and prioritized fixes", which targets the single-GPU per-token
+// decode step (its CUDA-graph item, roadmap E9).
 //
 // Work split.  One CTA of 16 warps per SM.  CTA c owns a contiguous range of
 // output columns (whole 16-column blocks for the SwiGLU epilogues, whose

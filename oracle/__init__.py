@@ -227,6 +227,32 @@ def gemm(a_codes, a_sf, g_a, w_codes, w_sf, g_w, residual=None):
     return ref, absref, out
 
 
+def gemm_id(a_codes, a_sf, g_a, w_codes, w_sf, g_w, ids):
+    """Expert-indexed GEMM (a mixture-of-experts layer's routed projection):
+    for token t and routing slot j, row [t, j] is the GEMM row of A[t] with
+    the weights of expert ids[t, j], with that expert's global scale:
+      out[t, j, n] = bf16( fp32(g_a * g_w[e]) * sum_k A[t, k] W_e[n, k] ),  e = ids[t, j].
+    w_codes uint8 [E, N, K/2], w_sf logical uint8 [E, N, K/16], g_w [E],
+    ids int [T, k] in [0, E).  Each expert's rows go through `gemm`.
+    Returns (ref fp64 [T, k, N], absref fp64 [T, k, N], out bf16 bits [T, k, N])."""
+    ids = np.asarray(ids)
+    T, kk = ids.shape
+    E, N = w_codes.shape[0], w_codes.shape[1]
+    assert ids.min() >= 0 and ids.max() < E and a_codes.shape[0] == T
+    ref = np.zeros((T, kk, N), np.float64)
+    absref = np.zeros((T, kk, N), np.float64)
+    out = np.zeros((T, kk, N), np.uint16)
+    for e in range(E):
+        t_idx, j_idx = np.nonzero(ids == e)
+        if t_idx.size == 0:
+            continue
+        r, ar, o = gemm(a_codes[t_idx], a_sf[t_idx], g_a, w_codes[e], w_sf[e], g_w[e])
+        ref[t_idx, j_idx] = r
+        absref[t_idx, j_idx] = ar
+        out[t_idx, j_idx] = o
+    return ref, absref, out
+
+
 # --------------------------------------------------------- norm / SwiGLU
 def rmsnorm(x_bits, w_bits, eps=1e-6):
     x = _c(x_bits, np.uint16)

@@ -12,7 +12,7 @@ import torch
 import synthetic
 from conftest import read_golden
 
-E2M1 = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+from _decode import E2M1, dequant_independent, e4m3_torch  # noqa: F401  (decode shared by the pins)
 
 
 def bf16(v):
@@ -23,18 +23,27 @@ def f32(b):
     return synthetic.bf16_bits_to_f32(b).astype(np.float64)
 
 
-def e4m3_torch(byte_array):
-    return torch.from_numpy(np.asarray(byte_array, np.uint8)).view(torch.float8_e4m3fn).to(torch.float64).numpy()
-
-
-def dequant_independent(codes, sf, g):
-    """Decode with the golden E2M1 table and torch's E4M3 decode."""
-    codes = np.asarray(codes, np.uint8)
-    lo, hi = codes & 15, codes >> 4
-    nib = np.stack([lo, hi], -1).reshape(codes.shape[0], -1)
-    val = np.where(nib & 8, -1.0, 1.0) * E2M1[nib & 7]
-    scale = np.repeat(e4m3_torch(sf), 16, axis=1)
-    return val * scale * float(g)
+# ------------------------------------------------------------- dequantize
+def test_dequantize_matches_independent_decode(oracle_mod):
+    """The oracle's element decode against the golden-table / torch-cast
+    decode: every code at every finite scale byte, in both nibbles, with a
+    non-trivial global scale."""
+    sc = np.arange(0x7F, dtype=np.uint8)                # every non-NaN E4M3 byte
+    rows = sc.size
+    # codes: byte j of a 16-element block holds codes (2j, 2j+1); cover all
+    # 16 codes in both nibbles across the row
+    lo = np.arange(16, dtype=np.uint8)
+    hi = (lo * 7 + 3) % 16
+    block = (lo[:8] | (hi[:8] << 4)).astype(np.uint8)
+    block2 = (lo[8:] | (hi[8:] << 4)).astype(np.uint8)
+    codes = np.tile(np.concatenate([block, block2]), (rows, 1))     # 32 elements per row
+    sf = np.stack([sc, sc[::-1]], axis=1)                           # two blocks per row
+    g = float(np.float32(0.0123))
+    got = oracle_mod.dequantize(codes, sf, g)
+    want = dequant_independent(codes, sf, np.float32(g))
+    assert np.array_equal(got, want)
+    # a sign or nibble-order slip shows up: element 1 of row 1 is code hi[0]
+    assert got[1, 1] == (-1.0 if hi[0] & 8 else 1.0) * E2M1[hi[0] & 7] * e4m3_torch([1])[0] * np.float32(g)
 
 
 # --------------------------------------------------------------- quantize

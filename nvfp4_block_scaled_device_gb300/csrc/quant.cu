@@ -50,23 +50,98 @@ __device__ __forceinline__ FF ff_add(FF a, FF b)
     return {h, __fsub_rn(s.lo, __fsub_rn(h, s.hi))};
 }
 
-__device__ __forceinline__ FF ff_sumsq8(FF acc, const uint4& p)
+// Pairs of binary32 values in one 64-bit register, for the packed f32x2
+// arithmetic of sm_100-class GPUs (each lane rounded to nearest, as the
+// scalar operation): element 0 in the low half.
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b)
 {
-    float f[8];
-    unpack8(p, f);
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b)
+{
+    uint64_t r;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b)
+{
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t f2_dup(float a)
+{
+    return ((uint64_t)__float_as_uint(a) << 32) | __float_as_uint(a);
+}
+// two bf16 (element 0 in the low half of w) -> their binary32 values (exact)
+__device__ __forceinline__ uint64_t bf16x2_f2(uint32_t w)
+{
+    return ((uint64_t)(w & 0xFFFF0000u) << 32) | (uint64_t)(w << 16);
+}
+__device__ __forceinline__ float f2_lo(uint64_t v) { return __uint_as_float((uint32_t)v); }
+__device__ __forceinline__ float f2_hi(uint64_t v) { return __uint_as_float((uint32_t)(v >> 32)); }
+
+// Two float-float sums side by side (the element pairs' even and odd
+// members): the error-free additions of ff_add_f on f32x2 registers.
+struct FF2 {
+    uint64_t hi, lo;
+};
+
+__device__ __forceinline__ FF2 ff2_add_f2(FF2 a, uint64_t p)
+{
+    const uint64_t s = f2_add(a.hi, p);
+    const uint64_t bp = f2_sub(s, a.hi);
+    const uint64_t e = f2_add(f2_sub(a.hi, f2_sub(s, bp)), f2_sub(p, bp));
+    return {s, f2_add(a.lo, e)};
+}
+
+__device__ __forceinline__ FF2 ff2_sumsq8(FF2 acc, const uint4& p)
+{
+    const uint32_t w[4] = {p.x, p.y, p.z, p.w};
 #pragma unroll
-    for (int i = 0; i < 8; i++) acc = ff_add_f(acc, __fmul_rn(f[i], f[i]));   // bf16^2 is exact
+    for (int i = 0; i < 4; i++) {
+        const uint64_t v = bf16x2_f2(w[i]);
+        acc = ff2_add_f2(acc, f2_mul(v, v));            // bf16^2 is exact
+    }
     return acc;
 }
 
-// y = bf16( (x * r) * w ), one rounding per step.
-__device__ __forceinline__ void norm8(float* f, float r, const uint4& wp)
+// the two chains of an FF2, even member first
+__device__ __forceinline__ FF ff2_sum(FF2 a)
 {
-    float w[8];
-    unpack8(wp, w);
-#pragma unroll
-    for (int i = 0; i < 8; i++) f[i] = bf16_round(__fmul_rn(__fmul_rn(f[i], r), w[i]));
+    return ff_add(FF{f2_lo(a.hi), f2_lo(a.lo)}, FF{f2_hi(a.hi), f2_hi(a.lo)});
 }
+
+// y = bf16( (x * r) * w ) of 8 bf16 values, one rounding per step (packed).
+__device__ __forceinline__ uint4 norm8p(const uint4& xp, uint64_t r2, const uint4& wp)
+{
+    const uint32_t x[4] = {xp.x, xp.y, xp.z, xp.w};
+    const uint32_t w[4] = {wp.x, wp.y, wp.z, wp.w};
+    uint32_t y[4];
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+        const uint64_t t = f2_mul(f2_mul(bf16x2_f2(x[i]), r2), bf16x2_f2(w[i]));
+        asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(y[i]) : "f"(f2_hi(t)), "f"(f2_lo(t)));
+    }
+    return make_uint4(y[0], y[1], y[2], y[3]);
+}
+
+// Running max of |bf16| over packed pairs (exact; no NaN among the inputs).
+__device__ __forceinline__ uint32_t amax_bf16x8(uint32_t m, const uint4& p)
+{
+    uint32_t r = m;
+    const uint32_t w[4] = {p.x, p.y, p.z, p.w};
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+        uint32_t a;
+        asm("abs.bf16x2 %0, %1;" : "=r"(a) : "r"(w[i]));
+        asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(r), "r"(a));
+    }
+    return r;
+}
+__device__ __forceinline__ float amax_bf16x2_value(uint32_t m) { return fmaxf(bf16_lo(m), bf16_hi(m)); }
 
 // A row is shared by kWarpsPerRow warps: warp q of the row takes the
 // 256-column groups q, q + kWarpsPerRow, ... (group j = vectors 32j..32j+31,
@@ -86,16 +161,17 @@ struct RowShared {
 };
 
 // Float-float sum of squares of this lane's vectors in its warp's share of
-// the row (two independent chains over the even and the odd vectors, then
-// combined), shuffle-reduced over the warp (fixed order).
+// the row (four independent chains: the even and the odd vectors, each as
+// the even and the odd elements of its pairs, then combined in that order),
+// shuffle-reduced over the warp (fixed order).
 __device__ __forceinline__ FF warp_sumsq(const uint4* __restrict__ b, int ng)
 {
-    FF p0{0.0f, 0.0f}, p1{0.0f, 0.0f};
+    FF2 p0{0, 0}, p1{0, 0};
     for (int k = 0; k < ng; k += 2) {
-        p0 = ff_sumsq8(p0, b[k]);
-        if (k + 1 < ng) p1 = ff_sumsq8(p1, b[k + 1]);
+        p0 = ff2_sumsq8(p0, b[k]);
+        if (k + 1 < ng) p1 = ff2_sumsq8(p1, b[k + 1]);
     }
-    FF part = ff_add(p0, p1);
+    FF part = ff_add(ff2_sum(p0), ff2_sum(p1));
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
         FF other{__shfl_xor_sync(0xffffffffu, part.hi, o), __shfl_xor_sync(0xffffffffu, part.lo, o)};
@@ -178,12 +254,15 @@ __device__ __forceinline__ void vec_step(float* f, int64_t v, bool valid, int64_
 // *amax.  The amax and the quantize kernels both go through here, so the
 // RMSNorm they compute is bit-identical.  The block's barrier is executed
 // by every warp (NORM only), whatever its row.
-template <bool NORM, bool QUANT>
+// HAVE_R: the row's 1 / rms is given (r_in; no sum of squares, no block
+// barrier); otherwise computed and, if r_out is set, stored there by one
+// lane of the row.
+template <bool NORM, bool QUANT, bool HAVE_R = false>
 __device__ __forceinline__ void row_share(const uint4* __restrict__ xr, int64_t row, bool row_valid, int rb, int q,
                                           int64_t nvec, int64_t cols, const uint4* __restrict__ w, float eps,
                                           float g, uint8_t* __restrict__ codes, int64_t ld_codes,
                                           uint8_t* __restrict__ sf, int64_t kb_pad, __nv_bfloat16* __restrict__ y_out,
-                                          float* amax, RowShared& sh)
+                                          float* amax, RowShared& sh, float r_in = 1.0f, float* r_out = nullptr)
 {
     const int lane = threadIdx.x & 31;
     const int64_t ngroups = (nvec + 31) / 32;
@@ -196,7 +275,8 @@ __device__ __forceinline__ void row_share(const uint4* __restrict__ xr, int64_t 
             b[k] = (k < ng && v < nvec) ? xr[v] : make_uint4(0, 0, 0, 0);
         }
         float r = 1.0f;
-        if (NORM) {
+        if (NORM && HAVE_R) r = r_in;
+        if (NORM && !HAVE_R) {
             const FF part = warp_sumsq(b, kRegGroups);   // zero padding adds exact zeros
             if (lane == 0) {
                 sh.hi[rb][q] = part.hi;
@@ -206,6 +286,7 @@ __device__ __forceinline__ void row_share(const uint4* __restrict__ xr, int64_t 
             // one lane per warp (binary64 is slow on this GPU), then broadcast
             if (row_valid && lane == 0) r = row_inv_rms(sh, rb, cols, __frcp_rn((float)cols), eps);
             r = __shfl_sync(0xffffffffu, r, 0);
+            if (r_out && q == 0 && lane == 0) *r_out = r;
             __syncthreads();                            // sh is reused by the block's next rows
         }
 #pragma unroll
@@ -214,20 +295,21 @@ __device__ __forceinline__ void row_share(const uint4* __restrict__ xr, int64_t 
             const int64_t v = (int64_t)(q + k * kWarpsPerRow) * 32 + lane;
             const bool valid = v < nvec;                // uniform over each group of 8 lanes
             float f[8];
-            unpack8(b[k], f);
-            if (NORM && valid) norm8(f, r, w[v]);
+            unpack8((NORM && valid) ? norm8p(b[k], f2_dup(r), w[v]) : b[k], f);
             vec_step<NORM, QUANT>(f, v, valid, row, cols, g, codes, ld_codes, sf, kb_pad, y_out, amax);
         }
         return;
     }
     // long rows: sum of squares over the share, then the share again
     float r = 1.0f;
-    if (NORM) {
-        FF part{0.0f, 0.0f};
+    if (NORM && HAVE_R) r = r_in;
+    if (NORM && !HAVE_R) {
+        FF2 acc{0, 0};
         for (int k = 0; k < ng; k++) {
             const int64_t v = (int64_t)(q + k * kWarpsPerRow) * 32 + lane;
-            part = ff_sumsq8(part, v < nvec ? xr[v] : make_uint4(0, 0, 0, 0));
+            acc = ff2_sumsq8(acc, v < nvec ? xr[v] : make_uint4(0, 0, 0, 0));
         }
+        FF part = ff2_sum(acc);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
             FF other{__shfl_xor_sync(0xffffffffu, part.hi, o), __shfl_xor_sync(0xffffffffu, part.lo, o)};
@@ -240,14 +322,15 @@ __device__ __forceinline__ void row_share(const uint4* __restrict__ xr, int64_t 
         __syncthreads();
         if (lane == 0) r = row_inv_rms(sh, rb, cols, __frcp_rn((float)cols), eps);
         r = __shfl_sync(0xffffffffu, r, 0);
+        if (r_out && q == 0 && lane == 0) *r_out = r;
         __syncthreads();
     }
     for (int k = 0; k < ng; k++) {
         const int64_t v = (int64_t)(q + k * kWarpsPerRow) * 32 + lane;
         const bool valid = v < nvec;
         float f[8];
-        unpack8(v < nvec ? xr[v] : make_uint4(0, 0, 0, 0), f);
-        if (NORM && valid) norm8(f, r, w[v]);
+        const uint4 xv = v < nvec ? xr[v] : make_uint4(0, 0, 0, 0);
+        unpack8((NORM && valid) ? norm8p(xv, f2_dup(r), w[v]) : xv, f);
         vec_step<NORM, QUANT>(f, v, valid, row, cols, g, codes, ld_codes, sf, kb_pad, y_out, amax);
     }
 }
@@ -343,10 +426,15 @@ constexpr int kDepartWord = 48;    // byte 192
 
 // Block-wide amax of the per-thread values, merged into ws[0]; then the grid
 // barrier; returns the global scale to every thread of the block, or -1 if
-// the barrier wait gave up (status recorded).  Block 0 writes *g_out.
+// the barrier wait gave up (status recorded).  Block 0 writes *g_out.  One
+// thread per block touches the words: an atomicMax of the amax, then an
+// arrival whose release orders it before the count; the blocks poll the
+// count with acquire loads, spaced out so that the polls do not crowd the
+// arrivals at the word's L2 slice.  NT: threads of the block.
+template <int NT>
 __device__ float grid_global_scale(float amax, uint32_t* ws, float* g_out, int* status, int site)
 {
-    __shared__ float wmax[kRowThreads / 32];
+    __shared__ float wmax[NT / 32];
     __shared__ float s_g;
     const int wib = threadIdx.x >> 5;
 #pragma unroll
@@ -354,11 +442,10 @@ __device__ float grid_global_scale(float amax, uint32_t* ws, float* g_out, int* 
     if ((threadIdx.x & 31) == 0) wmax[wib] = amax;
     __syncthreads();
     if (threadIdx.x == 0) {
-        for (int w = 1; w < kRowThreads / 32; w++) amax = fmaxf(amax, wmax[w]);
+        for (int w = 1; w < NT / 32; w++) amax = fmaxf(amax, wmax[w]);
         // non-negative binary32 values order like their bit patterns
         atomicMax(&ws[0], __float_as_uint(amax));
-        __threadfence();
-        atomicAdd(&ws[kArriveWord], 1u);
+        asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(ws + kArriveWord) : "memory");
         const uint64_t t0 = clock64();
         float g = -1.0f;
         for (;;) {
@@ -374,60 +461,87 @@ __device__ float grid_global_scale(float amax, uint32_t* ws, float* g_out, int* 
                 if (status) atomicCAS(status, 0, kErrTimeout * 100 + site);
                 break;
             }
-            __nanosleep(64);
-        }
-        if (g >= 0.0f) {
-            if (blockIdx.x == 0) g_out[0] = g;
-            // every block has read the amax before it departs: the last one
-            // to depart clears the words for the next call
-            __threadfence();
-            if (atomicAdd(&ws[kDepartWord], 1u) == gridDim.x - 1) {
-                atomicExch(&ws[0], 0u);
-                atomicExch(&ws[kArriveWord], 0u);
-                atomicExch(&ws[kDepartWord], 0u);
-            }
+            __nanosleep(128);
         }
         s_g = g;
     }
     __syncthreads();
-    return s_g;
+    const float g = s_g;
+    if (threadIdx.x == 0 && g >= 0.0f) {
+        // off the block's path to its second phase: block 0 publishes the
+        // scale; every block has read the amax before it departs, and the
+        // last one to depart clears the words for the next call
+        if (blockIdx.x == 0) g_out[0] = g;
+        uint32_t before;
+        asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(before) : "l"(ws + kDepartWord) : "memory");
+        if (before == gridDim.x - 1) {
+            atomicExch(&ws[0], 0u);
+            atomicExch(&ws[kArriveWord], 0u);
+            atomicExch(&ws[kDepartWord], 0u);
+        }
+    }
+    return g;
 }
 
 // Scale rows [rows, pad128(rows)) of the swizzled layout must be zero.  The
 // last 128-row tile of the layout is one contiguous run of bytes: before the
 // grid barrier the whole grid clears it with 16-byte stores, and the
 // quantization after the barrier writes the tile's real rows over it.
+template <int NT>
 __device__ __forceinline__ void zero_last_scale_tile(uint8_t* __restrict__ sf, int64_t rows, int64_t kb_pad)
 {
     if (rows % 128 == 0) return;
     uint4* t = reinterpret_cast<uint4*>(sf + (rows / 128) * (kb_pad / 4) * 512);
     const int64_t n = kb_pad * 8;                        // (kb_pad / 4) tiles of 32 vectors
-    for (int64_t i = (int64_t)blockIdx.x * kRowThreads + threadIdx.x; i < n; i += (int64_t)gridDim.x * kRowThreads)
+    for (int64_t i = (int64_t)blockIdx.x * NT + threadIdx.x; i < n; i += (int64_t)gridDim.x * NT)
         t[i] = make_uint4(0, 0, 0, 0);
 }
 
-// Resident variant: one block per row pair (the grid covers every row at
-// once) and each warp's share of its row (at most kResGroups 256-column
-// groups) stays in registers across the barrier: the row is read once, its
-// RMSNorm computed once and held as bf16 for the quantizer.
+// Resident variant: every row is held by one block at once (up to kResRows
+// rows per block of kResThreads threads, row rb of block b being row
+// b + rb * gridDim.x, so the rows spread evenly over the SMs) and each warp's
+// share of its row (at most kResGroups 256-column groups) stays in registers
+// across the barrier: the row is read once, its RMSNorm computed once and
+// held as bf16 for the quantizer.  Few large blocks keep the grid barrier's
+// arrivals few.
 constexpr int kResGroups = 5;
 constexpr int kResMaxCols = kWarpsPerRow * kResGroups * 256;   // 5120
+constexpr int kResThreads = 1024;
+constexpr int kResRows = kResThreads / 32 / kWarpsPerRow;     // 8
+
+struct ResShared {
+    float hi[kResRows][kWarpsPerRow];
+    float lo[kResRows][kWarpsPerRow];
+};
+
+// row_inv_rms over a ResShared (the same combination order as RowShared).
+__device__ __forceinline__ float res_inv_rms(const ResShared& sh, int rb, int64_t cols, float rcp_n, float eps)
+{
+    FF t{sh.hi[rb][0], sh.lo[rb][0]};
+#pragma unroll
+    for (int q = 1; q < kWarpsPerRow; q++) t = ff_add(t, FF{sh.hi[rb][q], sh.lo[rb][q]});
+    const float n = (float)cols;                        // exact: cols < 2^24
+    const float q0 = div_by_n(t.hi, n, rcp_n);
+    const float rem = __fmaf_rn(-q0, n, t.hi);          // exact
+    const float ms = __fadd_rn(q0, div_by_n(__fadd_rn(rem, t.lo), n, rcp_n));
+    return __frcp_rn(__fsqrt_rn(__fadd_rn(ms, eps)));
+}
 
 template <bool NORM>
-__global__ void __launch_bounds__(kRowThreads, 4)
+__global__ void __launch_bounds__(kResThreads, 1)
     scale_quantize_resident_kernel(const __nv_bfloat16* __restrict__ x, int64_t rows, int64_t cols, int64_t ldx,
                                    const __nv_bfloat16* __restrict__ norm_w, float eps, float* __restrict__ g_out,
                                    uint8_t* __restrict__ codes, int64_t ld_codes, uint8_t* __restrict__ sf,
                                    uint32_t* __restrict__ ws, int* status)
 {
     griddep_launch_dependents();   // a following GEMM may be scheduled early
-    __shared__ RowShared sh;
-    __shared__ uint4 w_sh[NORM ? kResMaxCols / 8 : 1];   // the RMSNorm weight, for both rows
+    __shared__ ResShared sh;
+    __shared__ uint4 w_sh[NORM ? kResMaxCols / 8 : 1];   // the RMSNorm weight, for all rows of the block
     const int64_t nvec = cols / 8;
     const int64_t kb_pad = cols / 16;
     const int lane = threadIdx.x & 31;
     const int wib = threadIdx.x >> 5, rb = wib / kWarpsPerRow, q = wib % kWarpsPerRow;
-    const int64_t row = (int64_t)blockIdx.x * kRowsPerBlock + rb;
+    const int64_t row = (int64_t)blockIdx.x + (int64_t)gridDim.x * rb;
     const bool ok = row < rows;
     const uint4* xr = reinterpret_cast<const uint4*>(x + (ok ? row : 0) * ldx);
     const uint4* w = reinterpret_cast<const uint4*>(norm_w);
@@ -443,11 +557,11 @@ __global__ void __launch_bounds__(kRowThreads, 4)
     if (NORM) {
         // the weight goes to shared memory by asynchronous copies, in flight
         // with the row's loads; the block barrier below makes it visible
-        for (int64_t i = threadIdx.x; i < nvec; i += kRowThreads)
+        for (int64_t i = threadIdx.x; i < nvec; i += kResThreads)
             asm volatile("cp.async.ca.shared.global [%0], [%1], 16;" ::"r"(smem_u32(&w_sh[i])), "l"(w + i) : "memory");
         asm volatile("cp.async.commit_group;" ::: "memory");
     }
-    zero_last_scale_tile(sf, rows, kb_pad);
+    zero_last_scale_tile<kResThreads>(sf, rows, kb_pad);
     float r = 1.0f;
     if (NORM) {
         const float rcp_n = __frcp_rn((float)cols);    // off the row's critical path
@@ -458,27 +572,21 @@ __global__ void __launch_bounds__(kRowThreads, 4)
         }
         asm volatile("cp.async.wait_all;" ::: "memory");
         __syncthreads();
-        if (ok && lane == 0) r = row_inv_rms(sh, rb, cols, rcp_n, eps);
+        if (ok && lane == 0) r = res_inv_rms(sh, rb, cols, rcp_n, eps);
         r = __shfl_sync(0xffffffffu, r, 0);
     }
     // phase 1: the row (normalised when NORM, kept as bf16) and its amax
-    float amax = 0.0f;
+    uint32_t amax2 = 0;                                  // packed bf16 running max of |y|
+    const uint64_t r2 = f2_dup(r);
 #pragma unroll
     for (int k = 0; k < kResGroups; k++) {
         if (k >= ng) break;                             // uniform over the warp
         const int64_t v = (int64_t)(q + k * kWarpsPerRow) * 32 + lane;
         if (v >= nvec) break;                           // uniform over each group of 8 lanes
-        float f[8];
-        unpack8(b[k], f);
-        if (NORM) {
-            norm8(f, r, w_sh[v]);
-            b[k] = make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
-                              pack_bf16x2(f[6], f[7]));
-        }
-#pragma unroll
-        for (int i = 0; i < 8; i++) amax = fmaxf(amax, fabsf(f[i]));
+        if (NORM) b[k] = norm8p(b[k], r2, w_sh[v]);
+        amax2 = amax_bf16x8(amax2, b[k]);
     }
-    const float g = grid_global_scale(amax, ws, g_out, status, 7);
+    const float g = grid_global_scale<kResThreads>(amax_bf16x2_value(amax2), ws, g_out, status, 7);
     if (g < 0.0f) return;
     // phase 2: quantize the held row
 #pragma unroll
@@ -493,7 +601,13 @@ __global__ void __launch_bounds__(kRowThreads, 4)
 }
 
 // General variant: blocks loop over the rows in both phases (the rows are
-// read twice, as by the two separate kernels).
+// read twice, as by the two separate kernels).  Phase 2 walks each block's
+// rows in the reverse order, so the rows read last in phase 1, still in L2,
+// come first; with RMSNorm, phase 1 keeps each row's 1 / rms in shared
+// memory (up to kStashIters row pairs per block), so phase 2 does not
+// recompute it.
+constexpr int kStashIters = 32;
+
 template <bool NORM>
 __global__ void __launch_bounds__(kRowThreads, 3)
     scale_quantize_kernel(const __nv_bfloat16* __restrict__ x, int64_t rows, int64_t cols, int64_t ldx,
@@ -503,35 +617,44 @@ __global__ void __launch_bounds__(kRowThreads, 3)
 {
     griddep_launch_dependents();   // a following GEMM may be scheduled early
     __shared__ RowShared sh;
+    __shared__ float r_sh[NORM ? kStashIters : 1][kRowsPerBlock];
     const int64_t nvec = cols / 8;
     const int64_t kb_pad = cols / 16;
     const int wib = threadIdx.x >> 5, rb = wib / kWarpsPerRow, q = wib % kWarpsPerRow;
-    zero_last_scale_tile(sf, rows, kb_pad);
+    const int64_t step = (int64_t)gridDim.x * kRowsPerBlock;
+    const int64_t first = (int64_t)blockIdx.x * kRowsPerBlock;
+    const int64_t iters = first < rows ? (rows - first + step - 1) / step : 0;   // row pairs of this block
+    zero_last_scale_tile<kRowThreads>(sf, rows, kb_pad);
     float amax = 0.0f;
-    for (int64_t r0 = (int64_t)blockIdx.x * kRowsPerBlock; r0 < rows; r0 += (int64_t)gridDim.x * kRowsPerBlock) {
-        const int64_t row = r0 + rb;
+    for (int64_t it = 0; it < iters; it++) {
+        const int64_t row = first + it * step + rb;
         const bool ok = row < rows;
         row_share<NORM, false>(reinterpret_cast<const uint4*>(x + (ok ? row : 0) * ldx), row, ok, rb, q, nvec, cols,
                                reinterpret_cast<const uint4*>(norm_w), eps, 0.0f, nullptr, 0, nullptr, 0, nullptr,
-                               &amax, sh);
+                               &amax, sh, 1.0f, (NORM && it < kStashIters) ? &r_sh[NORM ? it : 0][rb] : nullptr);
     }
-    const float g = grid_global_scale(amax, ws, g_out, status, 8);
+    const float g = grid_global_scale<kRowThreads>(amax, ws, g_out, status, 8);
     if (g < 0.0f) return;
-    for (int64_t r0 = (int64_t)blockIdx.x * kRowsPerBlock; r0 < rows; r0 += (int64_t)gridDim.x * kRowsPerBlock) {
-        const int64_t row = r0 + rb;
+    for (int64_t it = iters - 1; it >= 0; it--) {
+        const int64_t row = first + it * step + rb;
         const bool ok = row < rows;
-        row_share<NORM, true>(reinterpret_cast<const uint4*>(x + (ok ? row : 0) * ldx), row, ok, rb, q, nvec, cols,
-                              reinterpret_cast<const uint4*>(norm_w), eps, g, codes, ld_codes, sf, kb_pad, nullptr,
-                              nullptr, sh);
+        const uint4* xr = reinterpret_cast<const uint4*>(x + (ok ? row : 0) * ldx);
+        if (NORM && it < kStashIters)
+            row_share<NORM, true, true>(xr, row, ok, rb, q, nvec, cols, reinterpret_cast<const uint4*>(norm_w), eps, g,
+                                        codes, ld_codes, sf, kb_pad, nullptr, nullptr, sh, r_sh[NORM ? it : 0][rb]);
+        else
+            row_share<NORM, true>(xr, row, ok, rb, q, nvec, cols, reinterpret_cast<const uint4*>(norm_w), eps, g, codes,
+                                  ld_codes, sf, kb_pad, nullptr, nullptr, sh);
     }
 }
 
 template <typename... KArgs, typename... Args>
-cudaError_t launch_cooperative(void (*kernel)(KArgs...), unsigned grid, cudaStream_t stream, Args... args)
+cudaError_t launch_cooperative(void (*kernel)(KArgs...), unsigned grid, unsigned block, cudaStream_t stream,
+                               Args... args)
 {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(kRowThreads);
+    cfg.blockDim = dim3(block);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -543,10 +666,10 @@ cudaError_t launch_cooperative(void (*kernel)(KArgs...), unsigned grid, cudaStre
 }
 
 // Blocks of a kernel that can be resident on one SM at once.
-int blocks_per_sm(const void* kernel)
+int blocks_per_sm(const void* kernel, int threads)
 {
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, kRowThreads, 0) != cudaSuccess) return 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, 0) != cudaSuccess) return 0;
     return n;
 }
 
@@ -602,32 +725,34 @@ cudaError_t launch_scale_quantize(const __nv_bfloat16* x, int64_t rows, int64_t 
     if (e != cudaSuccess) return e;
     if (dev >= 64) return cudaErrorInvalidDevice;
     if (!have[dev]) {
-        occ[dev][0] = blocks_per_sm((const void*)scale_quantize_resident_kernel<false>);
-        occ[dev][1] = blocks_per_sm((const void*)scale_quantize_resident_kernel<true>);
-        occ[dev][2] = blocks_per_sm((const void*)scale_quantize_kernel<false>);
-        occ[dev][3] = blocks_per_sm((const void*)scale_quantize_kernel<true>);
+        occ[dev][0] = blocks_per_sm((const void*)scale_quantize_resident_kernel<false>, kResThreads);
+        occ[dev][1] = blocks_per_sm((const void*)scale_quantize_resident_kernel<true>, kResThreads);
+        occ[dev][2] = blocks_per_sm((const void*)scale_quantize_kernel<false>, kRowThreads);
+        occ[dev][3] = blocks_per_sm((const void*)scale_quantize_kernel<true>, kRowThreads);
         for (int i = 0; i < 4; i++)
             if (occ[dev][i] < 1) return cudaErrorInvalidConfiguration;
         have[dev] = true;
     }
     const bool norm = norm_w != nullptr;
-    const int64_t pairs = (rows + kRowsPerBlock - 1) / kRowsPerBlock;
-    const int64_t res_cap = (int64_t)occ[dev][norm ? 1 : 0] * num_sms;
-    if (cols <= kResMaxCols && pairs <= res_cap) {
-        const unsigned grid = (unsigned)pairs;
+    // resident: a grid of min(rows, resident blocks) blocks, each holding
+    // rows b, b + grid, ... (at most kResRows of them)
+    const int64_t res_blocks = (int64_t)occ[dev][norm ? 1 : 0] * num_sms;
+    if (cols <= kResMaxCols && rows <= res_blocks * kResRows) {
+        const unsigned grid = (unsigned)(rows < res_blocks ? rows : res_blocks);
         if (norm)
-            return launch_cooperative(scale_quantize_resident_kernel<true>, grid, stream, x, rows, cols, ldx, norm_w,
-                                      eps, g_out, codes, ld_codes, sf, ws, status);
-        return launch_cooperative(scale_quantize_resident_kernel<false>, grid, stream, x, rows, cols, ldx, norm_w,
-                                  eps, g_out, codes, ld_codes, sf, ws, status);
+            return launch_cooperative(scale_quantize_resident_kernel<true>, grid, kResThreads, stream, x, rows, cols,
+                                      ldx, norm_w, eps, g_out, codes, ld_codes, sf, ws, status);
+        return launch_cooperative(scale_quantize_resident_kernel<false>, grid, kResThreads, stream, x, rows, cols, ldx,
+                                  norm_w, eps, g_out, codes, ld_codes, sf, ws, status);
     }
+    const int64_t pairs = (rows + kRowsPerBlock - 1) / kRowsPerBlock;
     const int64_t cap = (int64_t)occ[dev][norm ? 3 : 2] * num_sms;
     const unsigned grid = (unsigned)(pairs < cap ? pairs : cap);
     if (norm)
-        return launch_cooperative(scale_quantize_kernel<true>, grid, stream, x, rows, cols, ldx, norm_w, eps, g_out,
-                                  codes, ld_codes, sf, ws, status);
-    return launch_cooperative(scale_quantize_kernel<false>, grid, stream, x, rows, cols, ldx, norm_w, eps, g_out,
-                              codes, ld_codes, sf, ws, status);
+        return launch_cooperative(scale_quantize_kernel<true>, grid, kRowThreads, stream, x, rows, cols, ldx, norm_w,
+                                  eps, g_out, codes, ld_codes, sf, ws, status);
+    return launch_cooperative(scale_quantize_kernel<false>, grid, kRowThreads, stream, x, rows, cols, ldx, norm_w, eps,
+                              g_out, codes, ld_codes, sf, ws, status);
 }
 
 }  // namespace nvfp4

@@ -345,6 +345,167 @@ def side_measurements(nv, W, stream, hbm_gbs, fp4_peak):
     return out
 
 
+# ------------------------------------------------ the other workloads
+def graph_time_us(fn, stream, n, reps=3):
+    """Mean device time of fn() over n launches captured in one CUDA graph
+    (best of `reps` replays, after one warm replay)."""
+    with torch.cuda.stream(stream):
+        fn()
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for _ in range(n):
+            fn()
+    best = None
+    with torch.cuda.stream(stream):
+        g.replay()
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+            e1.synchronize()
+            t = e0.elapsed_time(e1) * 1e3 / n
+            best = t if best is None else min(best, t)
+    return best
+
+
+def mlp_weight_bytes(h=H, i=I):
+    n = 3 * i * h
+    return n // 2 + n // 16
+
+
+def oracle_mlp_rate(T_list, budget_s=4.0):
+    """Oracle MLP tokens/s on the host cores (configs 2 and 5): each T with
+    T <= 17 timed in full; larger T extrapolated linearly from the T=17
+    per-token time (every MLP step after the two global scales is per token)."""
+    import oracle
+    oracle.build()
+    w = synthetic.mlp_weights(0, zero_block_frac=0.01)
+    q = {}
+    for k in ("gate", "up", "down"):
+        g = oracle.global_scale(w["w_" + k])
+        c, sf = oracle.quantize(w["w_" + k], g)
+        q[k] = (c, sf, g)
+    out = {}
+    per_token = None
+    for T in T_list:
+        if T <= 17:
+            x = synthetic.activations(T, seed=4, outliers=True)
+            t0 = time.perf_counter()
+            oracle.mlp(x, w["mlp_norm"], q["gate"], q["up"], q["down"])
+            el = time.perf_counter() - t0
+            out[T] = {"value": T / el, "how": f"timed in full ({el:.2f} s)"}
+            per_token = el / T
+        else:
+            out[T] = {"value": 1.0 / per_token, "how": "extrapolated linearly from the T=17 per-token time"}
+    return out, oracle.num_threads()
+
+
+def config_measurements(nv, W, blk_factory, stream, hbm_gbs, fp4_peak):
+    """Configs other than the headline one, each on its own workload and
+    reported with its roofline bound; timed as CUDA graphs of the launch
+    sets (device time, inputs resident)."""
+    dev = W["o"].codes.device
+    res = {}
+    # config 1: the single NVFP4 linear (16 x 512 x 256): latency-bound
+    a_bits, w_bits = synthetic.single_linear(16, 512, 256, seed=0)
+    to_dev = lambda b: torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).view(torch.bfloat16).to(dev)
+    ws = nv.workspace(256, dev)
+    A1, W1 = nv.quantize_new(to_dev(a_bits), ws), nv.quantize_new(to_dev(w_bits), ws)
+    o1 = torch.empty((16, 512), dtype=torch.bfloat16, device=dev)
+    us = graph_time_us(lambda: nv.nvfp4_gemm(A1, W1, o1, None, stream), stream, 200)
+    res["cfg1_single_linear_16x512x256"] = {"us_per_gemm": us, "TFLOP/s": 2 * 16 * 512 * 256 / us / 1e6,
+                                            "bound": "launch latency"}
+    # config 2: the decode MLP (T=1) as a graph; two layers' weights
+    # alternate so that each call streams its weights (300 MB > L2)
+    wb = {}
+    for layer in (0, 1):
+        m = synthetic.mlp_weights(layer)
+        wb[layer] = {k: nv.quantize_new(to_dev(m["w_" + k]), ws) for k in ("gate", "up", "down")}
+        wb[layer]["norm"] = to_dev(m["mlp_norm"])
+    x = to_dev(synthetic.activations(1, seed=1))
+    y = torch.empty_like(x)
+    gi = {l: torch.zeros(1, dtype=torch.float32, device=dev) for l in (0, 1)}
+    mws = nv.workspace(nv.mlp_workspace_bytes(1, H, I, nv.NVFP4_INTER_DYNAMIC), dev)
+    with torch.cuda.stream(stream):
+        for l in (0, 1):
+            nv.nvfp4_mlp(x, wb[l]["norm"], wb[l]["gate"], wb[l]["up"], wb[l]["down"], nv.NVFP4_INTER_DYNAMIC, gi[l],
+                         y, mws, True, 1e-6, stream)
+
+    def two_layers():
+        for l in (0, 1):
+            nv.nvfp4_mlp(x, wb[l]["norm"], wb[l]["gate"], wb[l]["up"], wb[l]["down"], nv.NVFP4_INTER_STATIC, gi[l],
+                         y, mws, True, 1e-6, stream)
+    us2 = graph_time_us(two_layers, stream, 50) / 2
+    wbytes = mlp_weight_bytes()
+    res["cfg2_decode_mlp_T1"] = {"us_per_mlp": us2, "tokens_per_s_per_layer": 1e6 / us2,
+                                 "weight_GB/s": wbytes / us2 / 1e3, "frac_of_hbm": wbytes / us2 / 1e3 / hbm_gbs,
+                                 "bound": "hbm", "launches": "3 per MLP, CUDA graph",
+                                 "weights": "two layers alternate (300 MB > L2)"}
+    del wb
+    # config 5: MLP T sweep, Student-t(3) activations with 0.1% of channels
+    # x100, weights with 1% all-zero blocks
+    m = synthetic.mlp_weights(0, zero_block_frac=0.01)
+    wz = {k: nv.quantize_new(to_dev(m["w_" + k]), ws) for k in ("gate", "up", "down")}
+    nz = to_dev(m["mlp_norm"])
+    sweep = {}
+    for T in (1, 3, 17, 128, 777, 4096, 8192):
+        xt = to_dev(synthetic.activations(T, seed=4, outliers=True))
+        yt = torch.empty_like(xt)
+        g5 = torch.zeros(1, dtype=torch.float32, device=dev)
+        w5 = nv.workspace(nv.mlp_workspace_bytes(T, H, I, nv.NVFP4_INTER_DYNAMIC), dev)
+        with torch.cuda.stream(stream):
+            nv.nvfp4_mlp(xt, nz, wz["gate"], wz["up"], wz["down"], nv.NVFP4_INTER_DYNAMIC, g5, yt, w5, True, 1e-6,
+                         stream)
+        n = max(2, min(50, int(2e4 / max(T, 1) ** 0.8)))
+        us5 = graph_time_us(lambda: nv.nvfp4_mlp(xt, nz, wz["gate"], wz["up"], wz["down"], nv.NVFP4_INTER_STATIC,
+                                                 g5, yt, w5, True, 1e-6, stream), stream, n)
+        flops = 2 * T * 3 * I * H
+        nbytes = wbytes + 45824 * T
+        t_roof = max(flops / (fp4_peak * 1e12), nbytes / (hbm_gbs * 1e9)) * 1e6
+        sweep[T] = {"us": us5, "tokens_per_s": T / us5 * 1e6, "TFLOP/s": flops / us5 / 1e6,
+                    "GB/s": nbytes / us5 / 1e3,
+                    "bound": "tensor" if flops / (fp4_peak * 1e12) > nbytes / (hbm_gbs * 1e9) else "hbm",
+                    "frac_of_roofline": t_roof / us5}
+        del xt, yt, w5
+    res["cfg5_mlp_T_sweep_outliers_zero_blocks"] = sweep
+    del wz
+    # config 4: T=16384 as 16 ubatches of 1024 through 8 stacked layers, ONE
+    # graph (capture fails on any host synchronisation: 0 per layer)
+    L, U, T = 8, 16, 1024
+    blocks = [blk_factory(layer) for layer in range(L)]
+    xs = [to_dev(synthetic.activations(T, seed=3 + 1000 * u)) for u in range(U)]
+    bufs = [[torch.empty((T, H), dtype=torch.bfloat16, device=dev) for _ in range(2)] for _ in range(U)]
+    with torch.cuda.stream(stream):
+        for b in blocks:
+            b.calibrate(xs[0], bufs[0][0], stream)
+
+    def all_layers():
+        for u in range(U):
+            inp = xs[u]
+            for layer in range(L):
+                out = bufs[u][layer % 2]
+                blocks[layer].forward(inp, out, stream)
+                inp = out
+    us4 = graph_time_us(all_layers, stream, 1, reps=3)
+    res["cfg4_long_prefill_T16384_8_layers"] = {
+        "ms_per_pass": us4 / 1e3, "tokens_per_s": U * T / us4 * 1e6,
+        "layer_tokens_per_s": L * U * T / us4 * 1e6, "TFLOP/s": L * U * block_flops(T) / us4 / 1e6,
+        "frac_of_fp4_peak": L * U * block_flops(T) / us4 / 1e6 / fp4_peak,
+        "host_syncs_per_layer": 0, "launches_per_pass": L * U * PrefillBlockLaunches(),
+        "how": "16 ubatches x 8 layers (seeded weights per layer) captured as one CUDA graph; a host "
+               "synchronisation anywhere in the launch set would fail the capture"}
+    del blocks, xs, bufs
+    torch.cuda.empty_cache()
+    return res
+
+
+def PrefillBlockLaunches():
+    from nvfp4_block_scaled_device_gb300.block import PrefillBlock
+    return PrefillBlock.LAUNCHES_PER_FORWARD
+
+
 # ----------------------------------------------------------- GPU (ours)
 def run_ours(args):
     import __graft_entry__
@@ -401,6 +562,8 @@ def run_ours(args):
                     nv.nvfp4_scale_quantize(x, blk.h, blk.ws_amax, blk.attn_norm, 1e-6, stream)
                 elif args.only == "step":
                     blk.forward_timed(x, out, ev, stream)
+                elif args.only == "mma_probe":
+                    log(f"[bench] MMA issue rate: {nv.mma_issue_rate():.0f} MAC/clk/SM")
         stream.synchronize()
         assert nv.device_status() == 0
         log(f"[bench] --only {args.only}: {args.only_reps} launches done")
@@ -500,11 +663,27 @@ def run_ours(args):
         if dist:
             dist.destroy_process_group()
         return
-    hbm_gbs, _, bf16_sust_peak, _ = peaks()
-    side = side_measurements(nv, W, stream, hbm_gbs, bf16_sust_peak * FP4_PER_BF16) if args.side else None
+    hbm_gbs, bf16_burst_peak, _, _ = peaks()
+    side = side_measurements(nv, W, stream, hbm_gbs, bf16_burst_peak * FP4_PER_BF16) if args.side else None
+    mma_rate = nv.mma_issue_rate()
+    clk_stats = clk
+    configs = None
+    if args.configs:
+        def blk_factory(layer):
+            aw = synthetic.attn_weights(layer)
+            mw = synthetic.mlp_weights(layer)
+            Wl = {}
+            for k, name, src in (("qkv", "w_qkv", aw), ("o", "w_o", aw), ("gate", "w_gate", mw), ("up", "w_up", mw),
+                                 ("down", "w_down", mw)):
+                Wl[k] = nv.quantize_new(to_dev(src[name]), ws)
+            return PrefillBlock(T, Wl, to_dev(aw["attn_norm"]), to_dev(mw["mlp_norm"]))
+        configs = config_measurements(nv, W, blk_factory, stream, hbm_gbs, bf16_burst_peak * FP4_PER_BF16)
+        assert nv.device_status() == 0
 
     hbm, bf16_burst, bf16_sust, src = peaks()
-    fp4_peak = bf16_sust * FP4_PER_BF16
+    # the timed region is milliseconds long: the burst figure applies
+    fp4_peak = bf16_burst * FP4_PER_BF16
+    fp4_sust = bf16_sust * FP4_PER_BF16
     gu_flops = 2 * T * 2 * I * H
     roofline = None
     if "gate_up_swiglu_us" in gemm:
@@ -512,7 +691,17 @@ def run_ours(args):
         roofline = {"bound": "tensor", "achieved": achieved, "peak": fp4_peak, "unit": "TFLOP/s",
                     "frac": achieved / fp4_peak, "traffic": recorded_traffic(),
                     "kernel": "fused gate/up GEMM + SwiGLU + FP4 requant (T=1024, N=2x17408, K=5120)",
-                    "peak_source": f"{src}: bf16 sustained {bf16_sust} TFLOP/s x {FP4_PER_BF16:g} (nominal FP4/BF16)"}
+                    "peak_source": f"{src}: bf16 burst {bf16_burst} TFLOP/s x {FP4_PER_BF16:g} (nominal FP4/BF16), "
+                                   "of measured",
+                    "peak_sustained": fp4_sust, "frac_of_sustained": achieved / fp4_sust}
+        if mma_rate:
+            sm_mhz = (clk_stats or {}).get("sm_mhz") or 2070.0
+            mma_peak = 2 * mma_rate * torch.cuda.get_device_properties(dev).multi_processor_count * sm_mhz * 1e6 / 1e12
+            roofline["mma_issue"] = {
+                "mac_per_clk_per_sm": mma_rate, "sm_mhz": sm_mhz, "peak_TFLOP/s": mma_peak,
+                "frac": achieved / mma_peak,
+                "how": "nvfp4_mma_issue_rate: the kernels' fused K-stage block (12 scale copies + 4 MMAs of "
+                       "256x256x64) issued back to back on one SM pair, operands in shared memory"}
     tflops = {}
     for k, fl in (("qkv", 2 * T * QKV * H), ("o", 2 * T * H * H), ("gate_up_swiglu", gu_flops),
                   ("down", 2 * T * H * I)):
@@ -539,10 +728,21 @@ def run_ours(args):
         "roofline": roofline,
         "e2e": e2e,
         "side": side,
+        "configs": configs,
         "clocks": clk,
     }
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wbits, x_bits, T)
+        if configs:
+            T_list = sorted(configs["cfg5_mlp_T_sweep_outliers_zero_blocks"])
+            rates, cores = oracle_mlp_rate(T_list)
+            for Tk in T_list:
+                configs["cfg5_mlp_T_sweep_outliers_zero_blocks"][Tk]["oracle_tokens_per_s"] = rates[Tk]
+            configs["cfg2_decode_mlp_T1"]["oracle_tokens_per_s"] = rates[1]
+            configs["cfg4_long_prefill_T16384_8_layers"]["oracle_tokens_per_s"] = {
+                "value": line["cpu_baseline"]["value"] / 8,
+                "how": "extrapolated: the oracle's per-token block rate over one layer (cpu_baseline) / 8 layers"}
+            configs["oracle_cores"] = cores
     print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()
@@ -558,7 +758,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-side", dest="side", action="store_false",
                     help="skip the side measurements (quantize at R=16384, GEMMs at T=1 and T=16384)")
-    ap.add_argument("--only", choices=("swiglu", "down", "qkv", "norm_quantize", "step"),
+    ap.add_argument("--no-configs", dest="configs", action="store_false",
+                    help="skip the other workloads (single linear, decode MLP, T sweep, 8-layer long prefill)")
+    ap.add_argument("--only", choices=("swiglu", "down", "qkv", "norm_quantize", "step", "mma_probe"),
                     help="profiling target: run one kernel of the step --only-reps times and exit")
     ap.add_argument("--only-reps", type=int, default=3)
     args = ap.parse_args()

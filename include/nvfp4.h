@@ -124,6 +124,16 @@ const char* nvfp4_status_string(int status);
  * the current device, which kernels set when a pipeline wait times out.
  * SYNCHRONOUS (a device-to-host copy); diagnostics and tests only. */
 int nvfp4_device_status(int* status_out, int clear);
+/* Measures the issue rate of the tensor-core instruction form the GEMM
+ * kernels use (tcgen05.mma.cta_group::2 kind::mxf4nvf4 scale_vec::4X,
+ * M=256 N=256 K=64, with its scale copies), fed back to back from operands
+ * already in shared memory on one SM pair of the current device: writes
+ * the multiply-adds per SM per clock cycle to *mac_per_clk.  Returns
+ * NVFP4_ERR_TIMEOUT if the measurement's bounded wait ran out.  SYNCHRONOUS;
+ * a measurement diagnostic (the dense NVFP4 peak of this instruction is
+ * 2 * mac_per_clk * SMs * SM clock), not part of the path.  No counterpart
+ * in the pages, which give no peak. */
+int nvfp4_mma_issue_rate(double* mac_per_clk);
 
 /* ------------------------------------------------------------- the path */
 

@@ -45,6 +45,7 @@ _SIGS = {
     "nvfp4_mlp_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int]),
     "nvfp4_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "nvfp4_device_status": (ctypes.c_int, [ctypes.POINTER(ctypes.c_int), ctypes.c_int]),
+    "nvfp4_mma_issue_rate": (ctypes.c_int, [ctypes.POINTER(ctypes.c_double)]),
     "nvfp4_amax_scale": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
                                         ctypes.c_void_p, ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p,
                                         ctypes.c_size_t, ctypes.c_void_p]),
@@ -152,6 +153,14 @@ def device_status(clear: bool = True) -> int:
     """Device-side status word (synchronous; diagnostics and tests)."""
     v = ctypes.c_int(0)
     _check(lib().nvfp4_device_status(ctypes.byref(v), int(clear)), "nvfp4_device_status")
+    return v.value
+
+
+def mma_issue_rate() -> float:
+    """Multiply-adds per SM per clock of the GEMMs' block-scaled MMA form,
+    measured on the current device (synchronous; a measurement diagnostic)."""
+    v = ctypes.c_double(0.0)
+    _check(lib().nvfp4_mma_issue_rate(ctypes.byref(v)), "nvfp4_mma_issue_rate")
     return v.value
 
 

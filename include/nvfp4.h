@@ -227,6 +227,40 @@ int nvfp4_gemm(const nvfp4_tensor_t* A, const nvfp4_tensor_t* W,
                void* out, int64_t ldo, const void* residual, int64_t ldr,
                void* workspace, size_t workspace_bytes, nvfp4_stream_t stream);
 
+/* Rotary embedding applied by nvfp4_gemm_rope (all pointers DEVICE). */
+typedef struct {
+    const int32_t* pos;   /* int32 [M]: position of each output row, in [0, positions) (not checked on the device) */
+    const float* cos_t;   /* fp32 [positions x table_ld]: cos of the angle of (position, pair i) at [p*table_ld + i] */
+    const float* sin_t;   /* fp32, the same layout: sin of that angle */
+    int64_t table_ld;     /* floats per table row, >= rope_dim / 2 */
+    int64_t positions;    /* rows of the tables, >= 1 */
+    int64_t col0;         /* first output column of the first rotated head; even */
+    int64_t heads;        /* rotated heads (col0 + heads * head_dim <= N) */
+    int64_t head_dim;     /* columns per head; even */
+    int64_t rope_dim;     /* rotated columns per head: the LAST rope_dim of each head; even, <= head_dim */
+    int inverse;          /* nonzero: the inverse rotation */
+} nvfp4_rope_t;
+
+/*
+ * nvfp4_gemm_rope -- nvfp4_gemm (no residual) with a rotary position
+ * embedding applied to its bf16 output in the GEMM's epilogue, e.g. the Q
+ * and K heads of a QKV projection.  Source: "PERFORMANCE -- verified
+ * hot-path audit and prioritized fixes", P5 (RoPE on the last rope_dim
+ * columns of each head, float32 arithmetic from bf16 and back) and the
+ * structural target "fuse RoPE into the Q/KV GEMM epilogue".
+ * In a rotated head, the pairs (e, o) = (y[2i], y[2i+1]) of the last rope_dim
+ * columns of y = nvfp4_gemm's bf16 output are rotated with
+ * c = cos_t[pos[m]*table_ld + i], s = sin_t[...]:
+ *   forward: e' = e*c - o*s,  o' = e*s + o*c;  inverse: e' = e*c + o*s,  o' = o*c - e*s
+ * each product, sum and difference one binary32 operation, then rounded to
+ * bf16; every other column is nvfp4_gemm's output.
+ *   A, W, out, ldo, workspace  as nvfp4_gemm.
+ *   rope     the embedding's tables and geometry (above).
+ */
+int nvfp4_gemm_rope(const nvfp4_tensor_t* A, const nvfp4_tensor_t* W, void* out, int64_t ldo,
+                    const nvfp4_rope_t* rope, void* workspace, size_t workspace_bytes,
+                    nvfp4_stream_t stream);
+
 /*
  * nvfp4_gemm_swiglu -- fused gate/up GEMM with SwiGLU epilogue and FP4
  * requantization into the down projection's activation format:

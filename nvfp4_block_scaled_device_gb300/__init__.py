@@ -36,6 +36,13 @@ class _TensorC(ctypes.Structure):
                 ("rows", ctypes.c_int64), ("cols", ctypes.c_int64), ("ld", ctypes.c_int64)]
 
 
+class _RopeC(ctypes.Structure):
+    _fields_ = [("pos", ctypes.c_void_p), ("cos_t", ctypes.c_void_p), ("sin_t", ctypes.c_void_p),
+                ("table_ld", ctypes.c_int64), ("positions", ctypes.c_int64), ("col0", ctypes.c_int64),
+                ("heads", ctypes.c_int64), ("head_dim", ctypes.c_int64), ("rope_dim", ctypes.c_int64),
+                ("inverse", ctypes.c_int)]
+
+
 _SIGS = {
     "nvfp4_codes_bytes": (ctypes.c_size_t, [ctypes.c_int64, ctypes.c_int64]),
     "nvfp4_sf_bytes": (ctypes.c_size_t, [ctypes.c_int64, ctypes.c_int64]),
@@ -59,6 +66,9 @@ _SIGS = {
     "nvfp4_gemm": (ctypes.c_int, [ctypes.POINTER(_TensorC), ctypes.POINTER(_TensorC), ctypes.c_void_p,
                                   ctypes.c_int64, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p,
                                   ctypes.c_size_t, ctypes.c_void_p]),
+    "nvfp4_gemm_rope": (ctypes.c_int, [ctypes.POINTER(_TensorC), ctypes.POINTER(_TensorC), ctypes.c_void_p,
+                                       ctypes.c_int64, ctypes.POINTER(_RopeC), ctypes.c_void_p, ctypes.c_size_t,
+                                       ctypes.c_void_p]),
     "nvfp4_gemm_swiglu": (ctypes.c_int, [ctypes.POINTER(_TensorC), ctypes.POINTER(_TensorC),
                                          ctypes.POINTER(_TensorC), ctypes.c_int, ctypes.c_void_p,
                                          ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
@@ -234,6 +244,25 @@ def nvfp4_gemm(A: NVFP4Tensor, W: NVFP4Tensor, out: torch.Tensor, residual=None,
     nbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     _check(lib().nvfp4_gemm(ctypes.byref(a), ctypes.byref(w), _ptr(out), ldo, _ptr(residual), ldr,
                             _ptr(workspace), nbytes, _stream(stream)), "nvfp4_gemm")
+
+
+def nvfp4_gemm_rope(A: NVFP4Tensor, W: NVFP4Tensor, out: torch.Tensor, pos: torch.Tensor, cos_t: torch.Tensor,
+                    sin_t: torch.Tensor, col0: int, heads: int, head_dim: int, rope_dim: int, inverse=False,
+                    stream=None, workspace=None):
+    """nvfp4_gemm with the rotary embedding in its epilogue.  pos: int32
+    [M] on the device; cos_t, sin_t: float32 [positions, >= rope_dim/2] on
+    the device (row-major, the same shape)."""
+    _, _, ldo = _bf16_2d(out, "out")
+    if pos.dtype != torch.int32 or cos_t.dtype != torch.float32 or sin_t.dtype != torch.float32:
+        raise TypeError("pos must be int32, cos_t and sin_t float32")
+    if cos_t.shape != sin_t.shape or cos_t.dim() != 2 or cos_t.stride(1) != 1 or sin_t.stride() != cos_t.stride():
+        raise ValueError("cos_t and sin_t must be row-major 2-D tensors of one shape")
+    r = _RopeC(pos.data_ptr(), cos_t.data_ptr(), sin_t.data_ptr(), cos_t.stride(0), cos_t.shape[0], col0, heads,
+               head_dim, rope_dim, int(bool(inverse)))
+    a, w = A.c(), W.c()
+    nbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib().nvfp4_gemm_rope(ctypes.byref(a), ctypes.byref(w), _ptr(out), ldo, ctypes.byref(r),
+                                 _ptr(workspace), nbytes, _stream(stream)), "nvfp4_gemm_rope")
 
 
 def nvfp4_gemm_swiglu(A: NVFP4Tensor, W_gate: NVFP4Tensor, W_up: NVFP4Tensor, inter_mode: int,

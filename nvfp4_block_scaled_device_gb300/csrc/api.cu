@@ -261,6 +261,10 @@ int current_device_sms()
     return sms <= kSplitMaxCtas ? sms : 0;
 }
 
+// nvfp4_gemm and nvfp4_gemm_rope (rope NULL: no rotary embedding).
+int run_linear(const nvfp4_tensor_t* A, const nvfp4_tensor_t* W, void* out, int64_t ldo, const void* residual,
+               int64_t ldr, const nvfp4_rope_t* rope, void* workspace, size_t workspace_bytes, nvfp4_stream_t stream);
+
 }  // namespace
 
 // Workspace layouts (all offsets 256-B aligned).  Without the trailing
@@ -399,6 +403,29 @@ int nvfp4_scale_quantize(const void* x, int64_t rows, int64_t cols, int64_t ldx,
 int nvfp4_gemm(const nvfp4_tensor_t* A, const nvfp4_tensor_t* W, void* out, int64_t ldo, const void* residual,
                int64_t ldr, void* workspace, size_t workspace_bytes, nvfp4_stream_t stream)
 {
+    return run_linear(A, W, out, ldo, residual, ldr, nullptr, workspace, workspace_bytes, stream);
+}
+
+int nvfp4_gemm_rope(const nvfp4_tensor_t* A, const nvfp4_tensor_t* W, void* out, int64_t ldo,
+                    const nvfp4_rope_t* rope, void* workspace, size_t workspace_bytes, nvfp4_stream_t stream)
+{
+    if (!rope || !rope->pos || !rope->cos_t || !rope->sin_t) return NVFP4_ERR_INVALID_ARG;
+    if (!aligned(rope->pos, 4) || !aligned(rope->cos_t, 4) || !aligned(rope->sin_t, 4)) return NVFP4_ERR_MISALIGNED;
+    if (rope->head_dim < 2 || rope->head_dim % 2 != 0 || rope->rope_dim < 2 || rope->rope_dim % 2 != 0 ||
+        rope->rope_dim > rope->head_dim || rope->col0 < 0 || rope->col0 % 2 != 0 || rope->heads < 0 ||
+        rope->table_ld < rope->rope_dim / 2 || rope->positions < 1 || !W ||
+        rope->col0 + rope->heads * rope->head_dim > W->rows)
+        return NVFP4_ERR_INVALID_ARG;
+    return run_linear(A, W, out, ldo, nullptr, 0, rope, workspace, workspace_bytes, stream);
+}
+
+}  // extern "C"
+
+namespace {
+
+int run_linear(const nvfp4_tensor_t* A, const nvfp4_tensor_t* W, void* out, int64_t ldo, const void* residual,
+               int64_t ldr, const nvfp4_rope_t* rope, void* workspace, size_t workspace_bytes, nvfp4_stream_t stream)
+{
     NVFP4_TRY(check_tensor(A));
     NVFP4_TRY(check_tensor(W));
     if (A->cols != W->cols || W->rows % 16 != 0) return NVFP4_ERR_INVALID_ARG;
@@ -428,6 +455,17 @@ int nvfp4_gemm(const nvfp4_tensor_t* A, const nvfp4_tensor_t* W, void* out, int6
     a.residual = static_cast<const __nv_bfloat16*>(residual);
     a.ldr = ldr;
     a.status = d->status;
+    if (rope) {
+        a.rope_pos = rope->pos;
+        a.rope_cos = rope->cos_t;
+        a.rope_sin = rope->sin_t;
+        a.rope_ld = rope->table_ld;
+        a.rope_col0 = rope->col0;
+        a.rope_heads = rope->heads;
+        a.rope_hd = rope->head_dim;
+        a.rope_rd = rope->rope_dim;
+        a.rope_inverse = rope->inverse ? 1 : 0;
+    }
     if (workspace) {
         uint8_t* ws = static_cast<uint8_t*>(workspace);
         const SplitScratch sp =
@@ -439,6 +477,10 @@ int nvfp4_gemm(const nvfp4_tensor_t* A, const nvfp4_tensor_t* W, void* out, int6
     NVFP4_CUDA(run_gemm(ma, mb, mb, a, ops, d, (cudaStream_t)stream));
     return NVFP4_OK;
 }
+
+}  // namespace
+
+extern "C" {
 
 int nvfp4_gemm_swiglu(const nvfp4_tensor_t* A, const nvfp4_tensor_t* W_gate, const nvfp4_tensor_t* W_up,
                       int inter_mode, float* g_inter, uint8_t* s_codes, int64_t ld_s_codes, uint8_t* s_sf,

@@ -16,6 +16,56 @@ __device__ __forceinline__ float silu_mul(float gate, float up)
     return __fmul_rn(__fdividef(gate, __fadd_rn(1.0f, __expf(-gate))), up);
 }
 
+// Rotary embedding of a row's bf16 outputs, pair by pair from an even
+// column: a cursor holds the rotated-head index and the column within the
+// head, so that no division runs per pair.  Each step rotates the pair
+// (e, o) at the cursor if it lies in the last rope_rd columns of a rotated
+// head, in binary32 steps on the bf16-rounded outputs:
+//   forward: e' = e*c - o*s, o' = e*s + o*c; inverse: e' = e*c + o*s, o' = o*c - e*s
+// ("PERFORMANCE -- verified hot-path audit" P5, RoPE fused into the Q/KV
+// projection's epilogue), then advances two columns.
+struct RopeCursor {
+    int32_t head;     // rotated-head index of the cursor column (outside [0, heads): none)
+    int32_t within;   // cursor column within its head (even)
+    const float* c;   // the cos / sin table row of the row's position
+    const float* s;
+};
+
+__device__ __forceinline__ RopeCursor rope_begin(const GemmArgs& a, int64_t row, int64_t n)
+{
+    RopeCursor k;
+    const int64_t rel = n - a.rope_col0;
+    const int64_t head = rel >= 0 ? rel / a.rope_hd : -((-rel + a.rope_hd - 1) / a.rope_hd);
+    k.head = (int32_t)head;
+    k.within = (int32_t)(rel - head * a.rope_hd);
+    const int64_t p = a.rope_pos[row];
+    k.c = a.rope_cos + p * a.rope_ld;
+    k.s = a.rope_sin + p * a.rope_ld;
+    return k;
+}
+
+__device__ __forceinline__ void rope_step(const GemmArgs& a, RopeCursor& k, float& e, float& o)
+{
+    const int32_t hd = (int32_t)a.rope_hd, nope = (int32_t)(a.rope_hd - a.rope_rd);
+    if (k.head >= 0 && k.head < a.rope_heads && k.within >= nope) {
+        const int32_t i = (k.within - nope) >> 1;
+        const float c = __ldg(k.c + i), s = __ldg(k.s + i);
+        const float ec = __fmul_rn(e, c), os = __fmul_rn(o, s), es = __fmul_rn(e, s), oc = __fmul_rn(o, c);
+        if (a.rope_inverse) {
+            e = __fadd_rn(ec, os);
+            o = __fsub_rn(oc, es);
+        } else {
+            e = __fsub_rn(ec, os);
+            o = __fadd_rn(es, oc);
+        }
+    }
+    k.within += 2;
+    if (k.within >= hd) {
+        k.within -= hd;
+        ++k.head;
+    }
+}
+
 // bf16 output rows can go out through a per-warp shared-memory staging area
 // of kEpiStageRows rows: a thread holds one row's 128 columns, so storing
 // them straight from registers makes every warp store touch 32 rows, which
@@ -56,6 +106,9 @@ __device__ __forceinline__ void epilogue_row(const GemmArgs& args, bool swiglu, 
             const int64_t n_base = nt * 256 + h * 128;
             __nv_bfloat16* orow = args.out + row * args.ldo;
             const __nv_bfloat16* rrow = args.residual ? args.residual + row * args.ldr : nullptr;
+            const bool rope = args.rope_pos != nullptr;
+            RopeCursor rk{};
+            if (rope) rk = rope_begin(args, row, n_base);
 #pragma unroll
             for (int jb = 0; jb < 128; jb += 32) {
                 uint4 rp[4];
@@ -68,10 +121,14 @@ __device__ __forceinline__ void epilogue_row(const GemmArgs& args, bool swiglu, 
                 for (int t = 0; t < 4; t++) {
                     const int j = jb + 8 * t;
                     const int64_t n = n_base + j;
-                    if (n < args.N) {
-                        float y[8];
+                    float y[8];
 #pragma unroll
-                        for (int i = 0; i < 8; i++) y[i] = bf16_round(__fmul_rn(v[j + i], alpha0));
+                    for (int i = 0; i < 8; i++) y[i] = bf16_round(__fmul_rn(v[j + i], alpha0));
+                    if (rope) {
+#pragma unroll
+                        for (int q = 0; q < 4; q++) rope_step(args, rk, y[2 * q], y[2 * q + 1]);
+                    }
+                    if (n < args.N) {
                         if (rrow) {
                             y[0] = __fadd_rn(bf16_lo(rp[t].x), y[0]);
                             y[1] = __fadd_rn(bf16_hi(rp[t].x), y[1]);
@@ -93,14 +150,25 @@ __device__ __forceinline__ void epilogue_row(const GemmArgs& args, bool swiglu, 
             }
         }
     } else if (!swiglu) {
-        // staged: t = bf16(alpha * acc) of this lane's row, packed
+        // staged: t = bf16(alpha * acc) of this lane's row (rotated), packed
+        const int64_t n_base = nt * 256 + h * 128;
         uint32_t pk[64];
+        if (args.rope_pos != nullptr && row < args.M) {
+            RopeCursor rk = rope_begin(args, row, n_base);
 #pragma unroll
-        for (int i = 0; i < 64; i++)
-            pk[i] = pack_bf16x2(bf16_round(__fmul_rn(v[2 * i], alpha0)), bf16_round(__fmul_rn(v[2 * i + 1], alpha0)));
+            for (int i = 0; i < 64; i++) {
+                float e = bf16_round(__fmul_rn(v[2 * i], alpha0)), o = bf16_round(__fmul_rn(v[2 * i + 1], alpha0));
+                rope_step(args, rk, e, o);
+                pk[i] = pack_bf16x2(e, o);
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 64; i++)
+                pk[i] = pack_bf16x2(bf16_round(__fmul_rn(v[2 * i], alpha0)),
+                                    bf16_round(__fmul_rn(v[2 * i + 1], alpha0)));
+        }
         const int lane = threadIdx.x & 31;
         const int64_t row0 = row - lane;                 // the warp's first row
-        const int64_t n_base = nt * 256 + h * 128;
         const int c = lane & 15;                         // 16-byte chunk (8 columns) of a staged row
         const int64_t n = n_base + 8 * c;
         constexpr int kRounds = 32 / kEpiStageRows;

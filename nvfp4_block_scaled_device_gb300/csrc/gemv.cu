@@ -24,8 +24,9 @@
 // decode step (its CUDA-graph item, roadmap E9).
 //
 // Work split.  One CTA of 16 warps per SM.  CTA c owns a contiguous range of
-// output columns (whole 16-column blocks for the SwiGLU epilogues, whose
-// requantization needs them); its weight rows (gate rows, then up rows, for
+// output columns (whole column pairs, which the rotary embedding rotates;
+// whole 16-column blocks for the SwiGLU epilogues, whose requantization
+// needs them); its weight rows (gate rows, then up rows, for
 // SwiGLU) are cut into units of 512 code bytes (1024 elements; 16 bytes per
 // lane), and warp w takes the contiguous unit range [w U/16, (w+1) U/16).
 // Each lane keeps kDepth units in flight in registers (loaded ahead of the
@@ -130,9 +131,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const DecodeParams pr
         C = (int)(16 * (b1 - b0));
         R = 2 * C;
     } else {
-        const int64_t c0 = (int64_t)blockIdx.x * args.N / gridDim.x, c1 = (int64_t)(blockIdx.x + 1) * args.N / gridDim.x;
-        n0 = c0;
-        C = (int)(c1 - c0);
+        // whole column pairs (the rotary embedding rotates pairs)
+        const int64_t np = args.N / 2;
+        const int64_t p0 = (int64_t)blockIdx.x * np / gridDim.x, p1 = (int64_t)(blockIdx.x + 1) * np / gridDim.x;
+        n0 = 2 * p0;
+        C = (int)(2 * (p1 - p0));
         R = C;
     }
     const int U = R * S;
@@ -292,14 +295,24 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const DecodeParams pr
     const float ga = *args.ga;
     const float alpha0 = __fmul_rn(ga, *args.gb0);
     if (!swiglu) {
-        // out = bf16(alpha * acc) [then bf16(residual + that)]; consecutive
-        // threads take consecutive columns
-        for (int t = threadIdx.x; t < kM * R; t += kThreads) {
-            const int m = t / R, r = t % R;
+        // out = bf16(alpha * acc) [rotated] [then bf16(residual + that)];
+        // consecutive threads take consecutive column pairs
+        const int pairs = R / 2;
+        for (int t = threadIdx.x; t < kM * pairs; t += kThreads) {
+            const int m = t / pairs, r = 2 * (t % pairs);
             const int64_t n = n0 + r;
-            float y = bf16_round(__fmul_rn(racc[r * kM + m], alpha0));
-            if (args.residual) y = __fadd_rn(__bfloat162float(args.residual[m * args.ldr + n]), y);
-            args.out[m * args.ldo + n] = __float2bfloat16_rn(y);
+            float y0 = bf16_round(__fmul_rn(racc[r * kM + m], alpha0));
+            float y1 = bf16_round(__fmul_rn(racc[(r + 1) * kM + m], alpha0));
+            if (args.rope_pos) {
+                RopeCursor rk = rope_begin(args, m, n);
+                rope_step(args, rk, y0, y1);
+            }
+            if (args.residual) {
+                const uint32_t q = *reinterpret_cast<const uint32_t*>(args.residual + m * args.ldr + n);
+                y0 = __fadd_rn(bf16_lo(q), y0);
+                y1 = __fadd_rn(bf16_hi(q), y1);
+            }
+            *reinterpret_cast<uint32_t*>(args.out + m * args.ldo + n) = pack_bf16x2(y0, y1);
         }
         return;
     }
@@ -368,11 +381,11 @@ DecodeShape decode_shape(const GemmArgs& a, int num_sms)
 {
     DecodeShape d{};
     const bool swiglu = a.epilogue != kEpiBf16;
-    const int64_t units = swiglu ? a.N / 16 : a.N;   // columns, or 16-column blocks
+    const int64_t units = swiglu ? a.N / 16 : a.N / 2;   // column pairs, or 16-column blocks
     d.grid = (int)(units < num_sms ? units : num_sms);
     d.segs = (int)((a.K + kUnitElems - 1) / kUnitElems);
     const int64_t per = (units + d.grid - 1) / d.grid;
-    const int64_t rmax = swiglu ? 32 * per : per;                  // weight rows of a CTA, at most
+    const int64_t rmax = swiglu ? 32 * per : 2 * per;              // weight rows of a CTA, at most
     const int64_t umax = (rmax * d.segs + kWarps - 1) / kWarps;    // units of a warp, at most
     d.slots = (int)((umax + 2 * d.segs - 2) / d.segs);             // rows a warp's range touches, at most
     d.smem = (size_t)a.M * d.segs * (kUnitElems + 64 * 4) + (size_t)kWarps * d.slots * a.M * 4 +

@@ -112,6 +112,16 @@ struct GemmArgs {
     // run ahead of griddep_wait(); zero: every load waits for that kernel
     // (which may be the one that wrote them) to complete
     int weights_early;
+    // rotary embedding of the bf16 output (kEpiBf16 without residual;
+    // rope_pos NULL: none).  In each of the rope_heads heads of rope_hd
+    // columns from column rope_col0, the last rope_rd columns form (even,
+    // odd) pairs rotated by the angles of table row rope_pos[row] (rope_cos,
+    // rope_sin: rope_ld floats a row); rope_inverse: the inverse rotation
+    const int32_t* rope_pos;
+    const float* rope_cos;
+    const float* rope_sin;
+    int64_t rope_ld, rope_col0, rope_heads, rope_hd, rope_rd;
+    int rope_inverse;
 };
 
 // Split-schedule workspace: a fixed block of ready flags (one per epilogue

@@ -81,6 +81,18 @@ def test_invalid_arguments_rejected_on_host(L):
     assert L.nvfp4_quantize(16, 4, 32, 32, NULL, 1e-6, 16, 16, 16, 128, NULL, NULL) == 1
     # amax: missing workspace
     assert L.nvfp4_amax_scale(16, 4, 64, 64, NULL, 1e-6, 16, NULL, 0, NULL) == 5
+    # gemm_rope: no embedding, odd column, rotated heads past N, rope_dim > head_dim, misaligned table
+    a = nv._TensorC(16, 128 * 16, 4, 16, 256, 128)
+    w = nv._TensorC(16, 128 * 16, 4, 512, 256, 128)
+    assert L.nvfp4_gemm_rope(ctypes.byref(a), ctypes.byref(w), 16, 512, NULL, NULL, 0, NULL) == 1
+    for bad in (dict(col0=1), dict(heads=5), dict(rope_dim=256), dict(rope_dim=3), dict(table_ld=31)):
+        f = dict(pos=16, cos_t=16, sin_t=16, table_ld=32, positions=8, col0=0, heads=4, head_dim=128, rope_dim=64,
+                 inverse=0)
+        f.update(bad)
+        r = nv._RopeC(**f)
+        assert L.nvfp4_gemm_rope(ctypes.byref(a), ctypes.byref(w), 16, 512, ctypes.byref(r), NULL, 0, NULL) == 1, bad
+    r = nv._RopeC(pos=16, cos_t=18, sin_t=16, table_ld=32, positions=8, col0=0, heads=4, head_dim=128, rope_dim=64)
+    assert L.nvfp4_gemm_rope(ctypes.byref(a), ctypes.byref(w), 16, 512, ctypes.byref(r), NULL, 0, NULL) == 2
     # mlp: bad inter mode
     t = nv._TensorC(16, 128, 4, 256, 256, 128)
     assert L.nvfp4_mlp(16, 4, 256, 256, 16, 1e-6, ctypes.byref(t), ctypes.byref(t), ctypes.byref(t), 7, 16,

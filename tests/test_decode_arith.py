@@ -75,11 +75,11 @@ def test_scale_bit_pattern_and_product_are_exact(oracle_mod):
 
 
 def decode_shape(N, K, swiglu, num_sms, warps=16, unit=1024):
-    units = N // 16 if swiglu else N
+    units = N // 16 if swiglu else N // 2        # 16-column blocks, or column pairs
     grid = min(units, num_sms)
     segs = (K + unit - 1) // unit
     per = (units + grid - 1) // grid
-    rmax = 32 * per if swiglu else per
+    rmax = 32 * per if swiglu else 2 * per
     umax = (rmax * segs + warps - 1) // warps
     slots = (umax + 2 * segs - 2) // segs
     return grid, segs, slots, rmax
@@ -101,7 +101,7 @@ def test_work_split_covers_each_unit_once(swiglu):
                 C = 16 * ((c + 1) * nb // grid - c * nb // grid)
                 R = 2 * C
             else:
-                C = (c + 1) * N // grid - c * N // grid
+                C = 2 * ((c + 1) * (N // 2) // grid - c * (N // 2) // grid)
                 R = C
             assert 1 <= R <= rmax
             cols += C

@@ -56,7 +56,7 @@ def run(nv, ws, T, N, K, col0, heads, hd, rd, inverse, seed, split=False, P=4096
 
 
 # the QKV projection: 40 Q heads + 8 K heads of 128 rotated, 8 V heads not
-@pytest.mark.parametrize("T", [1, 2, 5, 300, 1024])
+@pytest.mark.parametrize("T", [1, 2, 5, 17, 300, 1024])
 def test_rope_qkv(nv, ws, T):
     run(nv, ws, T, 7168, 5120, 0, 48, 128, 64, False, seed=T)
 

@@ -118,6 +118,10 @@ size_t nvfp4_swiglu_workspace_bytes(int64_t T, int64_t I, int inter_mode);
  * device; likewise, its last 128 KB per SM (the split schedule's) may be
  * left out. */
 size_t nvfp4_mlp_workspace_bytes(int64_t T, int64_t H, int64_t I, int inter_mode);
+/* Workspace of nvfp4_gemm_experts for T tokens, topk slots, K columns and E
+ * experts: the routing tables plus the expert-sorted operand (at most
+ * T*topk + 127*min(E, T*topk) rows, rounded up to 128, of K/2 + K/16 bytes). */
+size_t nvfp4_experts_workspace_bytes(int64_t T, int64_t topk, int64_t K, int64_t num_experts);
 /* Static description of a status code. */
 const char* nvfp4_status_string(int status);
 /* Reads (and if clear != 0 resets) the library's device-side status word of
@@ -260,6 +264,37 @@ typedef struct {
 int nvfp4_gemm_rope(const nvfp4_tensor_t* A, const nvfp4_tensor_t* W, void* out, int64_t ldo,
                     const nvfp4_rope_t* rope, void* workspace, size_t workspace_bytes,
                     nvfp4_stream_t stream);
+
+/*
+ * nvfp4_gemm_experts -- expert-indexed GEMM, the routed projection of a
+ * mixture-of-experts layer (llama.cpp's MUL_MAT_ID).  For token t and routing
+ * slot j < topk, with e = ids[t*topk + j]:
+ *   out[(t*topk + j) * ldo + n] = bf16( fp32(A->g[0] * W->g[e]) * sum_k A[t,k] W_e[n,k] ),
+ * the sum and the rounding as in nvfp4_gemm.  The routing table stays on
+ * the device: three launches (routing, gather of the routed rows into an
+ * expert-sorted operand, grouped tcgen05 GEMM over a tile table built on the
+ * device), no host synchronisation.  Sources: "CUDA: NVFP4 prefill on
+ * Blackwell leaves ~1.45x performance on the table" (the MUL_MAT_ID tests
+ * its patch passes); "PERFORMANCE -- verified hot-path audit and prioritized
+ * fixes" (the routed experts run without a host read of the routing table).
+ *   A            [T x K] quantized activations.
+ *   W            the E experts' weights stacked: rows E*N (expert e = rows
+ *                e*N .. e*N + N - 1), cols K; W->g points to fp32[E], expert
+ *                e's global scale.  N = W->rows / E, a multiple of 128.
+ *   num_experts  E, 1 .. 4096.
+ *   ids          DEVICE int32 [T * topk]: the expert of each (token, slot).
+ *                An id outside [0, E) leaves that output row unwritten and
+ *                records NVFP4_ERR_INVALID_ARG * 100 + 30 in the device
+ *                status word (nvfp4_device_status).
+ *   topk         routing slots per token, >= 1 (T * topk < 2^31).
+ *   out          bf16 [T*topk x N], row pitch ldo (elements).
+ *   workspace    nvfp4_experts_workspace_bytes(T, topk, K, E) bytes,
+ *                256-byte aligned; no zero-fill needed; not shared with a
+ *                call that may run at the same time.
+ */
+int nvfp4_gemm_experts(const nvfp4_tensor_t* A, const nvfp4_tensor_t* W, int64_t num_experts, const int32_t* ids,
+                       int64_t topk, void* out, int64_t ldo, void* workspace, size_t workspace_bytes,
+                       nvfp4_stream_t stream);
 
 /*
  * nvfp4_gemm_swiglu -- fused gate/up GEMM with SwiGLU epilogue and FP4

@@ -53,6 +53,11 @@ _SIGS = {
     "nvfp4_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "nvfp4_device_status": (ctypes.c_int, [ctypes.POINTER(ctypes.c_int), ctypes.c_int]),
     "nvfp4_mma_issue_rate": (ctypes.c_int, [ctypes.POINTER(ctypes.c_double)]),
+    "nvfp4_experts_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                                        ctypes.c_int64]),
+    "nvfp4_gemm_experts": (ctypes.c_int, [ctypes.POINTER(_TensorC), ctypes.POINTER(_TensorC), ctypes.c_int64,
+                                          ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int64,
+                                          ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
     "nvfp4_amax_scale": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
                                         ctypes.c_void_p, ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p,
                                         ctypes.c_size_t, ctypes.c_void_p]),
@@ -295,3 +300,21 @@ def nvfp4_mlp(x: torch.Tensor, norm_w: torch.Tensor, W_gate: NVFP4Tensor, W_up: 
     _check(lib().nvfp4_mlp(_ptr(x), T, H, ldx, _ptr(norm_w), eps, ctypes.byref(wg), ctypes.byref(wu),
                            ctypes.byref(wd), inter_mode, _ptr(g_inter), _ptr(out), ldo, int(bool(add_residual)),
                            _ptr(ws), ws.numel(), _stream(stream)), "nvfp4_mlp")
+
+
+def experts_workspace_bytes(T: int, topk: int, K: int, num_experts: int) -> int:
+    return int(lib().nvfp4_experts_workspace_bytes(T, topk, K, num_experts))
+
+
+def nvfp4_gemm_experts(A: NVFP4Tensor, W: NVFP4Tensor, num_experts: int, ids: torch.Tensor, out: torch.Tensor,
+                       ws: torch.Tensor, stream=None):
+    """Expert-indexed GEMM.  W: the experts' weights stacked (rows = E * N,
+    W.g fp32[E]); ids: CUDA int32 [T, topk] (or [T * topk]); out: bf16
+    [T * topk, N], row t * topk + j for token t, slot j."""
+    if ids.dtype != torch.int32 or not ids.is_cuda or not ids.is_contiguous():
+        raise ValueError("ids must be a contiguous CUDA int32 tensor")
+    topk = ids.shape[1] if ids.dim() == 2 else ids.numel() // A.rows
+    _, _, ldo = _bf16_2d(out, "out")
+    a, w = A.c(), W.c()
+    _check(lib().nvfp4_gemm_experts(ctypes.byref(a), ctypes.byref(w), num_experts, _ptr(ids), topk, _ptr(out), ldo,
+                                    _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)), "nvfp4_gemm_experts")

@@ -318,6 +318,12 @@ size_t nvfp4_mlp_workspace_bytes(int64_t T, int64_t H, int64_t I, int inter_mode
     return nvfp4::mlp_base_workspace_bytes(T, H, I, inter_mode) + split_partial_bytes(current_device_sms());
 }
 
+size_t nvfp4_experts_workspace_bytes(int64_t T, int64_t topk, int64_t K, int64_t num_experts)
+{
+    if (T < 1 || topk < 1 || K < 64 || num_experts < 1) return 0;
+    return nvfp4::experts_layout(T, topk, K, num_experts).total;
+}
+
 const char* nvfp4_status_string(int status)
 {
     switch (status) {
@@ -481,6 +487,35 @@ int run_linear(const nvfp4_tensor_t* A, const nvfp4_tensor_t* W, void* out, int6
 }  // namespace
 
 extern "C" {
+
+int nvfp4_gemm_experts(const nvfp4_tensor_t* A, const nvfp4_tensor_t* W, int64_t num_experts, const int32_t* ids,
+                       int64_t topk, void* out, int64_t ldo, void* workspace, size_t workspace_bytes,
+                       nvfp4_stream_t stream)
+{
+    NVFP4_TRY(check_tensor(A));
+    NVFP4_TRY(check_tensor(W));
+    const int64_t E = num_experts;
+    if (E < 1 || E > 4096 || topk < 1 || !ids || A->cols != W->cols || W->rows % E != 0)
+        return NVFP4_ERR_INVALID_ARG;
+    const int64_t N = W->rows / E, T = A->rows, K = A->cols;
+    if (N % 128 != 0 || T * topk >= ((int64_t)1 << 31)) return NVFP4_ERR_INVALID_ARG;
+    if (!aligned(ids, 4)) return NVFP4_ERR_MISALIGNED;
+    NVFP4_TRY(check_bf16_matrix(out, T * topk, N, ldo));
+    const ExpertsLayout L = experts_layout(T, topk, K, E);
+    if (!workspace || workspace_bytes < L.total) return NVFP4_ERR_WORKSPACE;
+    if (!aligned(workspace, 256)) return NVFP4_ERR_MISALIGNED;
+    DeviceInfo* d = nullptr;
+    NVFP4_TRY(device_info(&d));
+    NVFP4_TRY(encoder());
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    CUtensorMap ma, mb;
+    NVFP4_TRY(make_codes_map(&ma, ws + L.codes, L.max_rows, K / 2, K / 2));
+    NVFP4_TRY(make_codes_map(&mb, W->codes, W->rows, K / 2, W->ld));
+    NVFP4_CUDA(launch_experts(A->codes, A->ld, A->sf, A->g, T, K, W->codes, W->ld, W->sf, W->g, N, E, ids, topk,
+                              static_cast<__nv_bfloat16*>(out), ldo, ws, ma, mb, d->status, d->num_sms,
+                              (cudaStream_t)stream));
+    return NVFP4_OK;
+}
 
 int nvfp4_gemm_swiglu(const nvfp4_tensor_t* A, const nvfp4_tensor_t* W_gate, const nvfp4_tensor_t* W_up,
                       int inter_mode, float* g_inter, uint8_t* s_codes, int64_t ld_s_codes, uint8_t* s_sf,

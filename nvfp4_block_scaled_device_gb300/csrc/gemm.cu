@@ -220,7 +220,11 @@ __device__ __forceinline__ bool flag_wait_warp(const int* f, volatile int* abort
 
 // kSplit: the split schedule (its fix-up code is compiled into this
 // instantiation only; the whole-tile instantiation carries none of it).
-template <bool kSplit>
+// kGrouped: the expert-indexed mode (GemmArgs::grp_*; whole tiles, bf16
+// epilogue without residual): tile m of the device table takes its A rows
+// from the expert-sorted operand and its B rows from that expert's block of
+// the stacked weights, and each output row goes where the row map says.
+template <bool kSplit, bool kGrouped = false>
 __global__ void __launch_bounds__(kNumThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b0,
                 const __grid_constant__ CUtensorMap map_b1, const GemmArgs args)
@@ -236,7 +240,12 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     const int lane = threadIdx.x & 31;
     const bool swiglu = args.epilogue != kEpiBf16;
 
-    const int64_t num_m = (args.M + 127) / 128;
+    int64_t num_m = (args.M + 127) / 128;
+    if (kGrouped) {
+        // the tile table is written by the previous kernel of the stream
+        griddep_wait();
+        num_m = *reinterpret_cast<const volatile int*>(args.grp_count);
+    }
     const int64_t num_n = swiglu ? args.N / 128 : (args.N + 255) / 256;
     const int64_t num_tiles = num_m * num_n;
     const int num_kk = (int)(args.K / 64);
@@ -312,11 +321,23 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             int ks, ke;
             while (ok && next_segment(sched, tile, ks, ke)) {
                 const int64_t mt = tile % num_m, nt = tile / num_m;
-                const int32_t ya = (int32_t)(mt * 128);
+                int32_t ya = (int32_t)(mt * 128);
                 int32_t yb0, yb1;
                 const uint8_t *pb0, *pb1;
                 bool has_b1;
-                if (swiglu) {
+                int64_t b_base = 0;        // grouped: first row of the tile's expert in the stacked weights
+                if (kGrouped) {
+                    const int4 td = args.grp_tiles[mt];
+                    ya = td.y;
+                    b_base = (int64_t)td.x * args.N;
+                }
+                if (kGrouped) {
+                    yb0 = (int32_t)(b_base + nt * 256);
+                    yb1 = yb0 + 128;
+                    pb0 = args.sfb0 + (b_base / 128 + 2 * nt) * args.sfb_tile_stride;
+                    pb1 = pb0 + args.sfb_tile_stride;
+                    has_b1 = nt * 256 + 128 < args.N;
+                } else if (swiglu) {
                     yb0 = yb1 = (int32_t)(nt * 128);
                     pb0 = args.sfb0 + nt * args.sfb_tile_stride;
                     pb1 = args.sfb1 + nt * args.sfb_tile_stride;
@@ -330,12 +351,14 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 }
                 const CUtensorMap* my_map = p < 2 ? &map_a : p < 4 ? &map_b0 : (swiglu ? &map_b1 : &map_b0);
                 const int32_t my_y = (p < 2 ? ya : p < 4 ? yb0 : yb1) + (p & 1) * kCodeBoxRows;
-                const bool my_box = p < 6 && my_y < (p < 2 ? args.M : args.N);
+                // bounds: B rows are checked within the (expert's) N rows
+                const int64_t yb0r = yb0 - b_base, yb1r = yb1 - b_base;
+                const bool my_box = p < 6 && (p < 2 ? my_y < args.M : my_y - b_base < args.N);
                 // code boxes of the stage that are fetched (A rows +64, B rows +64, +128, +192)
                 const uint32_t code_bytes =
-                    kBox * (1u + (ya + kCodeBoxRows < args.M ? 1u : 0u) + 1u + (yb0 + kCodeBoxRows < args.N ? 1u : 0u) +
-                            (yb1 < args.N ? 1u : 0u) + (yb1 + kCodeBoxRows < args.N ? 1u : 0u));
-                const uint8_t* pa = args.sfa + mt * args.sfa_tile_stride + (size_t)ks * 4 * kSfTile;
+                    kBox * (1u + (ya + kCodeBoxRows < args.M ? 1u : 0u) + 1u + (yb0r + kCodeBoxRows < args.N ? 1u : 0u) +
+                            (yb1r < args.N ? 1u : 0u) + (yb1r + kCodeBoxRows < args.N ? 1u : 0u));
+                const uint8_t* pa = args.sfa + (int64_t)(ya / 128) * args.sfa_tile_stride + (size_t)ks * 4 * kSfTile;
                 pb0 += (size_t)ks * 4 * kSfTile;
                 pb1 += (size_t)ks * 4 * kSfTile;
                 for (int kb = ks; kb < ke; kb++) {
@@ -490,6 +513,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         Schedule sched = make_schedule(num_tiles, num_kstages, split);
         int64_t tile;
         int ks, ke;
+        GemmArgs gargs = args;              // grouped: rows are output rows of the row map
+        if (kGrouped) gargs.M = args.grp_out_rows;
         while (next_segment(sched, tile, ks, ke)) {
             const int64_t mt = tile % num_m, nt = tile / num_m;
             if (!mbar_wait_warp<true>(smem_u32(&ctrl->acc_full), acc_ph, abort_flag, args.status, 4)) break;
@@ -626,8 +651,20 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             // direct stores (lower latency) for the exposed last epilogue
             // and in the split kernel (deep K: few, long segments)
             const bool last = sched.next >= sched.tiles;   // whole tiles: no tile follows
-            epilogue_row(args, swiglu, v, row, nt, h, alpha0, alpha1, g_inter, wamax,
-                         (!kSplit && !last) ? epi_stage : 0u);
+            if (kGrouped) {
+                // the tile's expert scale; the A row's output row (padding
+                // rows go past the last output row: not stored); each row
+                // stored by its own thread
+                const int4 td = args.grp_tiles[mt];
+                const int64_t arow = (int64_t)td.y + q * 32 + lane;
+                const int orow = args.grp_rowmap[arow];
+                const float alpha_e = __fmul_rn(ga, args.gb0[td.x]);
+                epilogue_row(gargs, false, v, orow >= 0 ? (int64_t)orow : args.grp_out_rows, nt, h, alpha_e, alpha_e,
+                             1.0f, wamax, 0u);
+            } else {
+                epilogue_row(args, swiglu, v, row, nt, h, alpha0, alpha1, g_inter, wamax,
+                             (!kSplit && !last) ? epi_stage : 0u);
+            }
             if (warp == kEpiWarp0 && lane == 0 && ecount == 1) TRACE_CTA(2);
             if (warp == kEpiWarp0 && lane == 0) TRACE_CTA(3);
         }
@@ -691,6 +728,23 @@ cudaError_t launch_gemm(const CUtensorMap& map_a, const CUtensorMap& map_b0, con
                                    map_a, map_b0, map_b1, args);
     return launch_programmatic(gemm_kernel<false>, dim3((unsigned)(tiles < num_sms ? tiles : num_sms)),
                                dim3(kNumThreads), kSmemBytes, stream, map_a, map_b0, map_b1, args);
+}
+
+cudaError_t launch_gemm_grouped(const CUtensorMap& map_a, const CUtensorMap& map_b, const GemmArgs& args, int num_sms,
+                                int64_t max_tiles, cudaStream_t stream)
+{
+    static int attr_set_for_device[64] = {0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 64 && !attr_set_for_device[dev]) {
+        e = cudaFuncSetAttribute(gemm_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        if (e != cudaSuccess) return e;
+        attr_set_for_device[dev] = 1;
+    }
+    const int64_t grid = max_tiles < num_sms ? max_tiles : num_sms;
+    return launch_programmatic(gemm_kernel<false, true>, dim3((unsigned)(grid > 0 ? grid : 1)), dim3(kNumThreads),
+                               kSmemBytes, stream, map_a, map_b, map_b, args);
 }
 
 }  // namespace nvfp4

@@ -122,6 +122,16 @@ struct GemmArgs {
     const float* rope_sin;
     int64_t rope_ld, rope_col0, rope_heads, rope_hd, rope_rd;
     int rope_inverse;
+    // grouped (expert-indexed) mode of the 1-SM kernel, from tables built on
+    // the device (launch_gemm_grouped): A is the expert-sorted operand of
+    // args.M rows (each expert's rows padded to 128); B the experts' weights
+    // stacked [E * N x K] (N per expert), gb0 fp32[E]; *grp_count M tiles,
+    // grp_tiles[m] = {expert, first A row, valid rows, 0}; an A row r goes
+    // to output row grp_rowmap[r] (< 0: padding); grp_out_rows output rows.
+    const int* grp_count;
+    const int4* grp_tiles;
+    const int* grp_rowmap;
+    int64_t grp_out_rows;
 };
 
 // Split-schedule workspace: a fixed block of ready flags (one per epilogue
@@ -138,6 +148,34 @@ inline size_t split_partial_bytes(int ctas) { return (size_t)ctas * (size_t)kSpl
 // box and 128-byte swizzle.
 cudaError_t launch_gemm(const CUtensorMap& map_a, const CUtensorMap& map_b0, const CUtensorMap& map_b1,
                         const GemmArgs& args, int num_sms, cudaStream_t stream);
+
+// Grouped mode of the 1-SM kernel (args.grp_* set, bf16 epilogue, no
+// residual, no split): a persistent grid of min(SMs, max_tiles) CTAs walks
+// the device tile table.
+cudaError_t launch_gemm_grouped(const CUtensorMap& map_a, const CUtensorMap& map_b, const GemmArgs& args, int num_sms,
+                                int64_t max_tiles, cudaStream_t stream);
+
+// Workspace of the expert-indexed GEMM (byte offsets): a 256-byte header of
+// int32 words ([0] M tiles, [1] rows of the expert-sorted operand, [2] an id
+// outside [0, E) was seen), per-expert counts, cursors, segment starts and
+// first tiles, the M-tile table (int4), the row map and source rows of the
+// sorted operand (int32), then that operand's codes and scales.  max_rows
+// bounds the sorted rows: pairs + 127 per expert that has any, rounded up to
+// 128.
+struct ExpertsLayout {
+    size_t counts, cursor, seg, tile_start, tiles, rowmap, src, codes, sf, total;
+    int64_t max_rows, max_tiles;
+};
+ExpertsLayout experts_layout(int64_t T, int64_t topk, int64_t K, int64_t E);
+
+// The three launches of the expert-indexed GEMM (routing, gather, grouped
+// GEMM); map_a covers the sorted operand's codes in the workspace, map_b the
+// stacked weights' codes (boxes of kCodeBoxRows rows).
+cudaError_t launch_experts(const uint8_t* a_codes, int64_t lda, const uint8_t* a_sf, const float* a_g, int64_t T,
+                           int64_t K, const uint8_t* w_codes, int64_t ldw, const uint8_t* w_sf, const float* w_g,
+                           int64_t N, int64_t E, const int32_t* ids, int64_t topk, __nv_bfloat16* out, int64_t ldo,
+                           uint8_t* ws, const CUtensorMap& map_a, const CUtensorMap& map_b, int* status, int num_sms,
+                           cudaStream_t stream);
 
 // SM-pair version (clusters of 2 CTAs, 256-row tiles): same arguments and
 // results, plus 1-D tensor maps of the scale factors of A, B0 and B1 (8-byte

@@ -113,3 +113,21 @@ def test_product_path_does_not_import_oracle():
                 src = open(os.path.join(dirpath, f)).read()
                 assert not re.search(r"^\s*(import|from)\s+oracle", src, flags=re.M), f
                 assert "liboracle" not in src and "nvfp4_oracle" not in src, f
+
+
+def test_experts_arguments_rejected_on_host(L):
+    import nvfp4_block_scaled_device_gb300 as nv
+    NULL = None
+    a = nv._TensorC(16, 128 * 16, 4, 16, 256, 128)
+    w = nv._TensorC(16, 128 * 16, 4, 4 * 256, 256, 128)
+    ids = ctypes.c_void_p(256)
+    # N = rows / E must be a multiple of 128; E >= 1; ids non-null
+    assert L.nvfp4_gemm_experts(ctypes.byref(a), ctypes.byref(w), 16, ids, 2, 16, 128, NULL, 0, NULL) == 1
+    assert L.nvfp4_gemm_experts(ctypes.byref(a), ctypes.byref(w), 0, ids, 2, 16, 128, NULL, 0, NULL) == 1
+    assert L.nvfp4_gemm_experts(ctypes.byref(a), ctypes.byref(w), 4, NULL, 2, 16, 128, NULL, 0, NULL) == 1
+    # no workspace
+    assert L.nvfp4_gemm_experts(ctypes.byref(a), ctypes.byref(w), 4, ids, 2, 16, 256, NULL, 0, NULL) == 5
+    # workspace size: routed rows padded per expert, codes + scales per row
+    b = nv.experts_workspace_bytes(16, 2, 256, 4)
+    assert b >= (32 + 127 * 4) // 128 * 128 * (128 + 16)
+    assert nv.experts_workspace_bytes(0, 2, 256, 4) == 0

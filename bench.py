@@ -471,6 +471,27 @@ def config_measurements(nv, W, blk_factory, stream, hbm_gbs, fp4_peak):
         del xt, yt, w5
     res["cfg5_mlp_T_sweep_outliers_zero_blocks"] = sweep
     del wz
+    # the routed-expert projection (next row: grouped GEMM for MoE experts):
+    # T=1024 tokens, top-4 of 64 experts, each expert 1536 x 5120, skewed
+    # routing (half of the tokens send a slot to expert 0); HBM-bound (the
+    # experts' 283 MB of weights stream once)
+    Tm, topk, E, Nm = 1024, 4, 64, 1536
+    rng = np.random.default_rng(8)
+    wx = nv.quantize_new(to_dev(synthetic.normal(rng, (E * Nm, H), std=0.02)), ws)
+    gx = torch.cat([nv.quantize_new(to_dev(synthetic.normal(rng, (Nm, H), std=0.02)), ws).g for _ in range(E)])
+    wx.g = gx                                           # per-expert global scales (values immaterial to timing)
+    ax = nv.quantize_new(to_dev(synthetic.activations(Tm, seed=9)), ws)
+    ids = np.stack([rng.choice(E, size=topk, replace=False) for _ in range(Tm)]).astype(np.int32)
+    ids[rng.random(Tm) < 0.5, 0] = 0
+    ids = torch.from_numpy(ids).to(dev)
+    ox = torch.empty((Tm * topk, Nm), dtype=torch.bfloat16, device=dev)
+    wsx = nv.workspace(nv.experts_workspace_bytes(Tm, topk, H, E), dev)
+    usx = graph_time_us(lambda: nv.nvfp4_gemm_experts(ax, wx, E, ids, ox, wsx, stream), stream, 20)
+    xbytes = E * Nm * H * 9 // 16
+    res["experts_T1024_top4_of_64_N1536_K5120"] = {
+        "us": usx, "TFLOP/s": 2 * Tm * topk * Nm * H / usx / 1e6, "weight_GB/s": xbytes / usx / 1e3,
+        "frac_of_hbm": xbytes / usx / 1e3 / hbm_gbs, "bound": "hbm", "launches": 3}
+    del wx, ax, ox, wsx
     # config 4: T=16384 as 16 ubatches of 1024 through 8 stacked layers, ONE
     # graph (capture fails on any host synchronisation: 0 per layer)
     L, U, T = 8, 16, 1024

@@ -220,11 +220,16 @@ int nvfp4_scale_quantize(const void* x, int64_t rows, int64_t cols, int64_t ldx,
  *            the GEMM may split its tiles' K ranges over all SMs when whole
  *            tiles would leave part of the GPU idle (fp32 partials combined
  *            in the workspace); otherwise whole tiles are spread over the SMs.
- * With M <= 2 and at most 32 MiB of weight codes the GEMM runs instead as a
- * weight stream on the CUDA cores (exact int32 sums of E2M1 code products
- * per 16-element block, block scales applied exactly in fp32, fp32
- * accumulation): the same result up to the fp32 summation order; the
- * workspace is not used.  nvfp4_gemm_swiglu and nvfp4_mlp do the same.
+ * With M <= 8 and such a workspace the GEMM runs instead as a weight stream
+ * on the tensor cores (the weights as the MMA's 128-row side, split over
+ * all SMs along K, fp32 partials combined in the workspace in a fixed
+ * order); without one, with M <= 2 and at most 32 MiB of weight codes, as
+ * a weight stream on the CUDA cores (exact int32 sums of E2M1 code
+ * products per 16-element block, block scales applied exactly in fp32,
+ * fp32 accumulation).  Either gives the same result up to the fp32
+ * summation order.  nvfp4_gemm_swiglu and nvfp4_mlp do the same, except
+ * that a SwiGLU GEMM whose 128-column blocks fill at least 85% of the SMs
+ * runs as whole tiles.
  * Requires K == A->cols == W->cols, K % 64 == 0, N % 16 == 0.
  */
 int nvfp4_gemm(const nvfp4_tensor_t* A, const nvfp4_tensor_t* W,

@@ -66,12 +66,13 @@ int encoder()
 }
 
 // 2-D byte tensor [rows x row_bytes], pitch ld, boxes of 128 bytes x
-// kCodeBoxRows rows, 128-B swizzle.
-int make_codes_map(CUtensorMap* m, const void* base, int64_t rows, int64_t row_bytes, int64_t ld)
+// box_rows rows, 128-B swizzle.
+int make_codes_map(CUtensorMap* m, const void* base, int64_t rows, int64_t row_bytes, int64_t ld,
+                   int box_rows = nvfp4::kCodeBoxRows)
 {
     cuuint64_t dims[2] = {(cuuint64_t)row_bytes, (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)ld};
-    cuuint32_t box[2] = {128, (cuuint32_t)nvfp4::kCodeBoxRows};
+    cuuint32_t box[2] = {128, (cuuint32_t)box_rows};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -145,7 +146,18 @@ constexpr int64_t kPairMinRows = 129;
 cudaError_t run_gemm(const CUtensorMap& ma, const CUtensorMap& mb0, const CUtensorMap& mb1, const GemmArgs& a,
                      const DecodeOperands& ops, const DeviceInfo* d, cudaStream_t stream)
 {
-    // one or two activation rows: a weight stream, on the CUDA cores
+    // a handful of activation rows: a weight stream, on the tensor cores
+    // given the split workspace (tickets and partials), else (one or two
+    // rows) on the CUDA cores.  A SwiGLU GEMM whose 128-column blocks
+    // nearly fill the GPU (>= 85% of the SMs) runs as whole tiles on the
+    // prefill kernel instead: no split-K partials to combine.
+    const bool whole_tiles = a.epilogue != kEpiBf16 && (a.N / 128) * 20 >= (int64_t)17 * d->num_sms;
+    if (!whole_tiles && decode_tc_eligible(a, d->num_sms)) {
+        CUtensorMap ma8;
+        if (make_codes_map(&ma8, ops.a_codes, a.M, a.K / 2, ops.lda, kDecodeTcMaxRows) != NVFP4_OK)
+            return cudaErrorInvalidValue;
+        return launch_decode_tc(ma8, mb0, mb1, a, d->num_sms, stream);
+    }
     if (gemv_eligible(a, d->num_sms)) return launch_gemv(ops, a, d->num_sms, stream);
     const bool swiglu = a.epilogue != kEpiBf16;
     const int64_t pair_tiles = (a.M + 255) / 256 * (swiglu ? a.N / 128 : (a.N + 255) / 256);
@@ -180,17 +192,13 @@ SplitScratch split_scratch(const DeviceInfo* d, uint8_t* flags, uint8_t* partial
     return sp;
 }
 
-int run_swiglu(const DeviceInfo* d, const nvfp4_tensor_t* A, const nvfp4_tensor_t* Wg, const nvfp4_tensor_t* Wu,
-               int mode, float* g_inter, uint8_t* s_codes, int64_t ld_s_codes, uint8_t* s_sf,
-               __nv_bfloat16* s_bf16_user, uint32_t* amax_ws, __nv_bfloat16* s_bf16_scratch, SplitScratch split,
-               bool weights_early, cudaStream_t stream)
+// The gate/up GEMM's arguments common to both SwiGLU modes (the caller
+// sets the epilogue and its outputs).
+GemmArgs swiglu_gemm_args(const DeviceInfo* d, const nvfp4_tensor_t* A, const nvfp4_tensor_t* Wg,
+                          const nvfp4_tensor_t* Wu, uint8_t* s_codes, int64_t ld_s_codes, uint8_t* s_sf,
+                          SplitScratch split, bool weights_early)
 {
     const int64_t T = A->rows, I = Wg->rows;
-    CUtensorMap ma, mg, mu;
-    NVFP4_TRY(make_codes_map(&ma, A->codes, T, A->cols / 2, A->ld));
-    NVFP4_TRY(make_codes_map(&mg, Wg->codes, I, Wg->cols / 2, Wg->ld));
-    NVFP4_TRY(make_codes_map(&mu, Wu->codes, I, Wu->cols / 2, Wu->ld));
-    const DecodeOperands ops = {A->codes, A->ld, Wg->codes, Wg->ld, Wu->codes, Wu->ld};
     GemmArgs a = {};
     a.M = T;
     a.N = I;
@@ -211,6 +219,21 @@ int run_swiglu(const DeviceInfo* d, const nvfp4_tensor_t* A, const nvfp4_tensor_
     a.s_kb_pad = pad_to(I / 16, 4);
     a.sk_flags = split.flags;
     a.sk_partials = split.partials;
+    return a;
+}
+
+int run_swiglu(const DeviceInfo* d, const nvfp4_tensor_t* A, const nvfp4_tensor_t* Wg, const nvfp4_tensor_t* Wu,
+               int mode, float* g_inter, uint8_t* s_codes, int64_t ld_s_codes, uint8_t* s_sf,
+               __nv_bfloat16* s_bf16_user, uint32_t* amax_ws, __nv_bfloat16* s_bf16_scratch, SplitScratch split,
+               bool weights_early, cudaStream_t stream)
+{
+    const int64_t T = A->rows, I = Wg->rows;
+    CUtensorMap ma, mg, mu;
+    NVFP4_TRY(make_codes_map(&ma, A->codes, T, A->cols / 2, A->ld));
+    NVFP4_TRY(make_codes_map(&mg, Wg->codes, I, Wg->cols / 2, Wg->ld));
+    NVFP4_TRY(make_codes_map(&mu, Wu->codes, I, Wu->cols / 2, Wu->ld));
+    const DecodeOperands ops = {A->codes, A->ld, Wg->codes, Wg->ld, Wu->codes, Wu->ld};
+    GemmArgs a = swiglu_gemm_args(d, A, Wg, Wu, s_codes, ld_s_codes, s_sf, split, weights_early);
     if (mode == NVFP4_INTER_STATIC) {
         a.epilogue = kEpiSwigluFp4;
         a.g_inter = g_inter;
@@ -598,9 +621,6 @@ int nvfp4_mlp(const void* x, int64_t T, int64_t H, int64_t ldx, const void* norm
                          s_bf16_scratch, split, true, st));
     // 4: down GEMM (+ residual)
     const nvfp4_tensor_t s = {s_codes, s_sf, g_inter, T, I, I / 2};
-    CUtensorMap ma, mb;
-    NVFP4_TRY(make_codes_map(&ma, s.codes, T, I / 2, I / 2));
-    NVFP4_TRY(make_codes_map(&mb, W_down->codes, H, I / 2, W_down->ld));
     GemmArgs a = {};
     a.epilogue = kEpiBf16;
     a.M = T;
@@ -620,6 +640,9 @@ int nvfp4_mlp(const void* x, int64_t T, int64_t H, int64_t ldx, const void* norm
     a.sk_flags = split.flags;
     a.sk_partials = split.partials;
     a.weights_early = 1;
+    CUtensorMap ma, mb;
+    NVFP4_TRY(make_codes_map(&ma, s.codes, T, I / 2, I / 2));
+    NVFP4_TRY(make_codes_map(&mb, W_down->codes, H, I / 2, W_down->ld));
     const DecodeOperands ops = {s.codes, I / 2, W_down->codes, W_down->ld, W_down->codes, W_down->ld};
     NVFP4_CUDA(run_gemm(ma, mb, mb, a, ops, d, st));
     return NVFP4_OK;

@@ -36,7 +36,7 @@
 // (deterministic), and runs the epilogue.  The activation rows are expanded
 // once per CTA into shared memory as int8 (2 x E2M1) and fp32 scales.
 #include "common.cuh"
-#include "gemm_epilogue.cuh"
+#include "decode_epilogue.cuh"
 #include "gemv.h"
 
 #ifndef NVFP4_DECODE_MAX_ROWS
@@ -292,83 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const DecodeParams pr
     __syncthreads();
 
     // ---- epilogue
-    const float ga = *args.ga;
-    const float alpha0 = __fmul_rn(ga, *args.gb0);
-    if (!swiglu) {
-        // out = bf16(alpha * acc) [rotated] [then bf16(residual + that)];
-        // consecutive threads take consecutive column pairs
-        const int pairs = R / 2;
-        for (int t = threadIdx.x; t < kM * pairs; t += kThreads) {
-            const int m = t / pairs, r = 2 * (t % pairs);
-            const int64_t n = n0 + r;
-            float y0 = bf16_round(__fmul_rn(racc[r * kM + m], alpha0));
-            float y1 = bf16_round(__fmul_rn(racc[(r + 1) * kM + m], alpha0));
-            if (args.rope_pos) {
-                RopeCursor rk = rope_begin(args, m, n);
-                rope_step(args, rk, y0, y1);
-            }
-            if (args.residual) {
-                const uint32_t q = *reinterpret_cast<const uint32_t*>(args.residual + m * args.ldr + n);
-                y0 = __fadd_rn(bf16_lo(q), y0);
-                y1 = __fadd_rn(bf16_hi(q), y1);
-            }
-            *reinterpret_cast<uint32_t*>(args.out + m * args.ldo + n) = pack_bf16x2(y0, y1);
-        }
-        return;
-    }
-    const float alpha1 = __fmul_rn(ga, *args.gb1);
-    const float g_inter = args.epilogue == kEpiSwigluFp4 ? *args.g_inter : 1.0f;
-    float wamax = 0.0f;
-    // s = bf16(silu(gate) * up), gate and up rounded to bf16 first; a thread
-    // takes 8 columns of one row, lanes 2q and 2q+1 one 16-column block
-    const int groups = kM * (C / 8);
-    for (int g0 = 0; g0 < groups; g0 += kThreads) {   // the same trip count for every thread
-        const int t = g0 + threadIdx.x;
-        const bool act = t < groups;
-        const int m = act ? t / (C / 8) : 0, i0 = act ? 8 * (t % (C / 8)) : 0;
-        float v[8];
-        float a8 = 0.0f;
-#pragma unroll
-        for (int k = 0; k < 8; k++) {
-            v[k] = 0.0f;
-            if (act) {
-                const float gate = bf16_round(__fmul_rn(racc[(i0 + k) * kM + m], alpha0));
-                const float up = bf16_round(__fmul_rn(racc[(C + i0 + k) * kM + m], alpha1));
-                v[k] = bf16_round(silu_mul(gate, up));
-                a8 = fmaxf(a8, fabsf(v[k]));
-            }
-        }
-        const float a16 = fmaxf(a8, __shfl_xor_sync(0xffffffffu, a8, 1));
-        if (act) {
-            const int64_t n = n0 + i0;
-            if (args.s_bf16) {
-                uint4 o;
-                o.x = pack_bf16x2(v[0], v[1]);
-                o.y = pack_bf16x2(v[2], v[3]);
-                o.z = pack_bf16x2(v[4], v[5]);
-                o.w = pack_bf16x2(v[6], v[7]);
-                *reinterpret_cast<uint4*>(args.s_bf16 + m * args.ld_s + n) = o;
-            }
-            if (args.epilogue == kEpiSwigluFp4) {
-                uint32_t sc;
-                const uint32_t cw = quant_half_block(v, g_inter, a16, &sc);
-                *reinterpret_cast<uint32_t*>(args.s_codes + m * args.ld_s_codes + n / 2) = cw;
-                if ((i0 & 8) == 0) args.s_sf[sf_offset(m, n / 16, args.s_kb_pad)] = (uint8_t)sc;
-            } else {
-                wamax = fmaxf(wamax, a8);
-            }
-        }
-    }
-    if (args.epilogue == kEpiSwigluFp4) {
-        // scale rows kM..127 of this CTA's blocks are padding: zero
-        const int nblk = C / 16;
-        for (int t = threadIdx.x; t < (128 - kM) * nblk; t += kThreads)
-            args.s_sf[sf_offset(kM + t / nblk, n0 / 16 + t % nblk, args.s_kb_pad)] = 0;
-    } else {
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) wamax = fmaxf(wamax, __shfl_xor_sync(0xffffffffu, wamax, o));
-        if (lane == 0) atomicMax(args.amax_ws, __float_as_uint(wamax));
-    }
+    decode_epilogue<kThreads>(args, epi_scalars(args), racc, kM, n0, C, threadIdx.x);
 }
 
 // Grid, slots and shared memory of one launch.

@@ -165,8 +165,8 @@ def pair_tile_rows(T, rng, extra=16):
     return np.unique(np.array(rows, np.int64))
 
 
-@pytest.mark.parametrize("T,outliers", [(1, False), (1024, False), (3, True), (777, True), (17, True), (128, True),
-                                        (4096, True), (8192, False)])
+@pytest.mark.parametrize("T,outliers", [(1, False), (2, False), (8, True), (1024, False), (3, True), (777, True),
+                                        (17, True), (128, True), (4096, True), (8192, False)])
 def test_mlp_full_size(nv, big_weights, big_weights_zb, T, outliers):
     """Decode (T=1) and prefill-ubatch (T=1024) MLP at H=5120, I=17408, and
     the T sweep with the outlier stress (Student-t(3) with 0.1% of channels

@@ -224,7 +224,8 @@ __device__ __forceinline__ bool flag_wait_warp(const int* f, volatile int* abort
 // epilogue without residual): tile m of the device table takes its A rows
 // from the expert-sorted operand and its B rows from that expert's block of
 // the stacked weights, and each output row goes where the row map says.
-template <bool kSplit, bool kGrouped = false>
+// kRope: the bf16 epilogue's rotary embedding compiled in (whole tiles only).
+template <bool kSplit, bool kGrouped = false, bool kRope = false>
 __global__ void __launch_bounds__(kNumThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b0,
                 const __grid_constant__ CUtensorMap map_b1, const GemmArgs args)
@@ -659,10 +660,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 const int64_t arow = (int64_t)td.y + q * 32 + lane;
                 const int orow = args.grp_rowmap[arow];
                 const float alpha_e = __fmul_rn(ga, args.gb0[td.x]);
-                epilogue_row(gargs, false, v, orow >= 0 ? (int64_t)orow : args.grp_out_rows, nt, h, alpha_e, alpha_e,
+                epilogue_row<false>(gargs, false, v, orow >= 0 ? (int64_t)orow : args.grp_out_rows, nt, h, alpha_e, alpha_e,
                              1.0f, wamax, 0u);
             } else {
-                epilogue_row(args, swiglu, v, row, nt, h, alpha0, alpha1, g_inter, wamax,
+                epilogue_row<kRope>(args, swiglu, v, row, nt, h, alpha0, alpha1, g_inter, wamax,
                              (!kSplit && !last) ? epi_stage : 0u);
             }
             if (warp == kEpiWarp0 && lane == 0 && ecount == 1) TRACE_CTA(2);
@@ -698,9 +699,13 @@ cudaError_t launch_gemm(const CUtensorMap& map_a, const CUtensorMap& map_b0, con
         if (e != cudaSuccess) return e;
         e = cudaFuncSetAttribute(gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
         if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(gemm_kernel<false, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kSmemBytes);
+        if (e != cudaSuccess) return e;
         attr_set_for_device[dev] = 1;
     }
     const bool swiglu = args.epilogue != kEpiBf16;
+    const bool rope = args.rope_pos != nullptr;
     const int64_t num_m = (args.M + 127) / 128;
     const int64_t num_n = swiglu ? args.N / 128 : (args.N + 255) / 256;
     const int64_t tiles = num_m * num_n;
@@ -718,7 +723,7 @@ cudaError_t launch_gemm(const CUtensorMap& map_a, const CUtensorMap& map_b0, con
     // its own load latency, so the idle SMs buy little, and the partials
     // and the split instantiation cost more.)
     const int64_t waves = (tiles + num_sms - 1) / num_sms;
-    const bool split = args.sk_partials != nullptr && args.sk_flags != nullptr && num_sms <= kSplitMaxCtas &&
+    const bool split = !rope && args.sk_partials != nullptr && args.sk_flags != nullptr && num_sms <= kSplitMaxCtas &&
                        tiles * stages >= num_sms && tiles * 10 < waves * num_sms * 9 && stages >= 32 &&
                        tiles * stages < (int64_t)1 << 31;
     // programmatic launch: the CTAs may start on SMs the previous kernel has
@@ -726,6 +731,9 @@ cudaError_t launch_gemm(const CUtensorMap& map_a, const CUtensorMap& map_b0, con
     if (split)
         return launch_programmatic(gemm_kernel<true>, dim3((unsigned)num_sms), dim3(kNumThreads), kSmemBytes, stream,
                                    map_a, map_b0, map_b1, args);
+    if (rope)
+        return launch_programmatic(gemm_kernel<false, false, true>, dim3((unsigned)(tiles < num_sms ? tiles : num_sms)),
+                                   dim3(kNumThreads), kSmemBytes, stream, map_a, map_b0, map_b1, args);
     return launch_programmatic(gemm_kernel<false>, dim3((unsigned)(tiles < num_sms ? tiles : num_sms)),
                                dim3(kNumThreads), kSmemBytes, stream, map_a, map_b0, map_b1, args);
 }

@@ -205,7 +205,8 @@ __device__ __forceinline__ bool flag_wait_warp2(const int* f, volatile int* abor
 
 // kSplit: the split schedule (its fix-up code is compiled into this
 // instantiation only).
-template <bool kSplit>
+// kRope: the bf16 epilogue's rotary embedding compiled in (whole tiles only).
+template <bool kSplit, bool kRope = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
     gemm2_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b0,
                  const __grid_constant__ CUtensorMap map_b1, const __grid_constant__ CUtensorMap map_sfa,
@@ -570,7 +571,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
             // staged bf16 stores while later tiles accumulate; direct stores
             // for the exposed last epilogue and in the split kernel
             const bool last = sched.next >= sched.tiles;   // whole tiles: no tile follows
-            epilogue_row(args, swiglu, v, row, nt, h, alpha0, alpha1, g_inter, wamax,
+            epilogue_row<kRope>(args, swiglu, v, row, nt, h, alpha0, alpha1, g_inter, wamax,
                          (!kSplit && !last) ? epi_stage : 0u);
         }
         if (args.epilogue == kEpiSwigluBf16) {
@@ -605,6 +606,8 @@ cudaError_t launch_gemm2(const CUtensorMap& map_a, const CUtensorMap& map_b0, co
         if (e != cudaSuccess) return e;
         e = cudaFuncSetAttribute(gemm2_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
         if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(gemm2_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        if (e != cudaSuccess) return e;
         attr_set_for_device[dev] = 1;
     }
     const bool swiglu = args.epilogue != kEpiBf16;
@@ -618,7 +621,8 @@ cudaError_t launch_gemm2(const CUtensorMap& map_a, const CUtensorMap& map_b0, co
     // and the tiles are deep in K (>= 32 stages): then every pair takes an
     // equal run of the (tile, K stage) units, as the 1-SM kernel's split.
     const int64_t waves = (tiles + all_pairs - 1) / all_pairs;
-    const bool split = args.sk_partials != nullptr && args.sk_flags != nullptr && num_sms <= kSplitMaxCtas &&
+    const bool rope = args.rope_pos != nullptr;
+    const bool split = !rope && args.sk_partials != nullptr && args.sk_flags != nullptr && num_sms <= kSplitMaxCtas &&
                        tiles * stages >= all_pairs && tiles * 10 < waves * all_pairs * 9 &&
                        stages >= kPairSplitMinStages &&
                        tiles * stages < (int64_t)1 << 31;
@@ -628,6 +632,9 @@ cudaError_t launch_gemm2(const CUtensorMap& map_a, const CUtensorMap& map_b0, co
     if (split)
         return launch_programmatic(gemm2_kernel<true>, dim3((unsigned)(2 * pairs)), dim3(kNumThreads), kSmemBytes,
                                    stream, map_a, map_b0, map_b1, map_sfa, map_sfb0, map_sfb1, args);
+    if (rope)
+        return launch_programmatic(gemm2_kernel<false, true>, dim3((unsigned)(2 * pairs)), dim3(kNumThreads),
+                                   kSmemBytes, stream, map_a, map_b0, map_b1, map_sfa, map_sfb0, map_sfb1, args);
     return launch_programmatic(gemm2_kernel<false>, dim3((unsigned)(2 * pairs)), dim3(kNumThreads), kSmemBytes, stream,
                                map_a, map_b0, map_b1, map_sfa, map_sfb0, map_sfb1, args);
 }

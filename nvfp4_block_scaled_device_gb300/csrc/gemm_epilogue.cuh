@@ -93,6 +93,10 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr)
 // call: every lane of the warp, rows >= M included); stage: this warp's
 // kEpiStageBytes of shared memory (shared-space address), or 0 for the
 // direct bf16 stores (lower latency: for an epilogue nothing overlaps).
+// kRope: the rotary embedding of the bf16 output (args.rope_*) is compiled
+// in; the kernels run that instantiation only for a call that asks for it,
+// so the others carry none of its code or registers.
+template <bool kRope>
 __device__ __forceinline__ void epilogue_row(const GemmArgs& args, bool swiglu, float (&v)[128], int64_t row,
                                              int64_t nt, int h, float alpha0, float alpha1, float g_inter,
                                              float& wamax, uint32_t stage)
@@ -106,9 +110,8 @@ __device__ __forceinline__ void epilogue_row(const GemmArgs& args, bool swiglu, 
             const int64_t n_base = nt * 256 + h * 128;
             __nv_bfloat16* orow = args.out + row * args.ldo;
             const __nv_bfloat16* rrow = args.residual ? args.residual + row * args.ldr : nullptr;
-            const bool rope = args.rope_pos != nullptr;
             RopeCursor rk{};
-            if (rope) rk = rope_begin(args, row, n_base);
+            if (kRope) rk = rope_begin(args, row, n_base);
 #pragma unroll
             for (int jb = 0; jb < 128; jb += 32) {
                 uint4 rp[4];
@@ -124,7 +127,7 @@ __device__ __forceinline__ void epilogue_row(const GemmArgs& args, bool swiglu, 
                     float y[8];
 #pragma unroll
                     for (int i = 0; i < 8; i++) y[i] = bf16_round(__fmul_rn(v[j + i], alpha0));
-                    if (rope) {
+                    if (kRope) {
 #pragma unroll
                         for (int q = 0; q < 4; q++) rope_step(args, rk, y[2 * q], y[2 * q + 1]);
                     }
@@ -153,7 +156,7 @@ __device__ __forceinline__ void epilogue_row(const GemmArgs& args, bool swiglu, 
         // staged: t = bf16(alpha * acc) of this lane's row (rotated), packed
         const int64_t n_base = nt * 256 + h * 128;
         uint32_t pk[64];
-        if (args.rope_pos != nullptr && row < args.M) {
+        if (kRope && row < args.M) {
             RopeCursor rk = rope_begin(args, row, n_base);
 #pragma unroll
             for (int i = 0; i < 64; i++) {

@@ -285,8 +285,9 @@ def side_measurements(nv, W, stream, hbm_gbs, fp4_peak):
     """After the timed region, outside the metric: the one-launch scale +
     quantize at R=16384 x K=5120 (168 MB of bf16 per pass; achieved GB/s on
     the algorithmic bytes 2RK read + 0.5625RK written) and every GEMM shape of
-    the block at T=1 (decode) and T=16384 (long prefill), with the block's
-    weights, each timed over a few launches with CUDA events."""
+    the block at T=1 (decode: weights streamed from HBM, launches in a CUDA
+    graph) and T=16384 (long prefill), with the block's weights, each timed
+    over a few launches with CUDA events."""
     def timed(fn, iters):
         with torch.cuda.stream(stream):
             fn()
@@ -313,7 +314,52 @@ def side_measurements(nv, W, stream, hbm_gbs, fp4_peak):
         out[name] = {"us": us, "GB/s": alg / us / 1e3, "frac_of_hbm": alg / us / 1e3 / hbm_gbs}
     del x, t
     gws = nv.workspace(nv.gemm_workspace_bytes(), dev)
-    for T in (1, 16384):
+    # T=1: each GEMM streams its weights from HBM, as a decode step does:
+    # launches back to back in a CUDA graph, cycling over copies of the
+    # weights that together exceed twice the L2
+    l2 = 129e6
+    A1 = {Kk: nv.NVFP4Tensor.empty(1, Kk, dev) for Kk in (H, I)}
+    for Kk, a in A1.items():
+        nv.nvfp4_scale_quantize(torch.randn((1, Kk), generator=gen, device=dev).bfloat16(), a, ws, None, 1e-6, stream)
+
+    def copies(Wt):
+        n = max(2, int(2.2 * l2 // (Wt.codes.numel() + Wt.sf.numel())) + 1)
+        return [nv.NVFP4Tensor(codes=Wt.codes.clone(), sf=Wt.sf.clone(), g=Wt.g.clone(), rows=Wt.rows, cols=Wt.cols)
+                for _ in range(n)]
+
+    def rotating_us(launch, n):
+        k = [0]
+
+        def fn():
+            launch(k[0] % n)
+            k[0] += 1
+        return graph_time_us(fn, stream, 4 * n)
+
+    res = {}
+    for name, Kk in (("qkv", H), ("o", H), ("down", I)):
+        Ws = copies(W[name])
+        o = torch.empty((1, W[name].rows), dtype=torch.bfloat16, device=dev)
+        us = rotating_us(lambda i: nv.nvfp4_gemm(A1[Kk], Ws[i], o, None, stream, gws), len(Ws))
+        b = W[name].codes.numel() + W[name].sf.numel()
+        res[name] = {"us": us, "TFLOP/s": 2 * W[name].rows * Kk / us / 1e6, "weight_GB/s": b / us / 1e3,
+                     "frac_of_hbm": b / us / 1e3 / hbm_gbs, "weight_copies": len(Ws)}
+        del Ws
+    Gs, Us = copies(W["gate"]), copies(W["up"])
+    s1 = nv.NVFP4Tensor.empty(1, I, dev)
+    g1 = torch.tensor([0.01], dtype=torch.float32, device=dev)
+    sws1 = nv.workspace(nv.swiglu_workspace_bytes(1, I, nv.NVFP4_INTER_STATIC), dev)
+    us = rotating_us(lambda i: nv.nvfp4_gemm_swiglu(A1[H], Gs[i], Us[i], nv.NVFP4_INTER_STATIC, g1, s1, sws1, None,
+                                                    stream), len(Gs))
+    b = sum(x_.codes.numel() + x_.sf.numel() for x_ in (W["gate"], W["up"]))
+    res["gate_up_swiglu"] = {"us": us, "TFLOP/s": 2 * 2 * I * H / us / 1e6, "weight_GB/s": b / us / 1e3,
+                             "frac_of_hbm": b / us / 1e3 / hbm_gbs, "weight_copies": len(Gs)}
+    del Gs, Us
+    for v in res.values():
+        v["frac_of_fp4_peak"] = v["TFLOP/s"] / fp4_peak
+    res["weights"] = "HBM-resident: launches cycle over weight copies > 2x L2"
+    out["gemm_T1"] = res
+    del A1
+    for T in (16384,):
         A = {Kk: nv.NVFP4Tensor.empty(T, Kk, dev) for Kk in (H, I)}
         for Kk, a in A.items():
             nv.nvfp4_scale_quantize(torch.randn((T, Kk), generator=gen, device=dev).bfloat16(), a, ws, None, 1e-6,
@@ -331,14 +377,6 @@ def side_measurements(nv, W, stream, hbm_gbs, fp4_peak):
         res["gate_up_swiglu"] = {"us": us, "TFLOP/s": 2 * T * 2 * I * H / us / 1e6}
         for v in res.values():
             v["frac_of_fp4_peak"] = v["TFLOP/s"] / fp4_peak
-        if T == 1:
-            wbytes = sum(Wt.codes.numel() + Wt.sf.numel() for Wt in W.values())
-            for name in res:
-                Wt = {"qkv": [W["qkv"]], "o": [W["o"]], "down": [W["down"]],
-                      "gate_up_swiglu": [W["gate"], W["up"]]}[name]
-                b = sum(x_.codes.numel() + x_.sf.numel() for x_ in Wt)
-                res[name]["weight_GB/s"] = b / res[name]["us"] / 1e3
-            res["weights_MB"] = wbytes / 1e6
         out[f"gemm_T{T}"] = res
         del A
     assert nv.device_status() == 0
@@ -527,6 +565,54 @@ def PrefillBlockLaunches():
     return PrefillBlock.LAUNCHES_PER_FORWARD
 
 
+# ------------------------------------------------ decode-kernel timeline
+def decode_timeline(nv, W, dev):
+    """Per-CTA timeline of the tensor-core decode GEMM at T=1 (QKV, O, down),
+    one cold launch each (L2 flushed, weights from HBM), from a library
+    built with the kernel's debug timeline (-DNVFP4_TRACE_DECODE; the
+    product library carries none of it).  Prints one JSON line per GEMM:
+    medians / maxima over the CTAs of the time (us from the first CTA's
+    entry) each reached a point, and per-CTA stall totals (us)."""
+    import ctypes
+    from nvfp4_block_scaled_device_gb300.build import build, PKG
+    path = build(extra_flags=["-DNVFP4_TRACE_DECODE"], out=os.path.join(PKG, "_build", "libnvfp4_trace.so"))
+    L = nv.lib(path)
+    L.nvfp4_debug_decode_trace.argtypes = [ctypes.c_void_p]
+    L.nvfp4_debug_decode_trace_clear.argtypes = []
+    nv._lib = L
+    names = ["entry", "setup_done", "first_stage_full", "last_segment_issued", "first_acc_full", "last_ticket",
+             "block_done", "exit"]
+    stalls = ["producer_wait_slot", "mma_wait_data", "mma_wait_acc", "epilogue_busy", "epi_store", "epi_ticket",
+              "epi_combine", "epi_block"]
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    gws = nv.workspace(nv.gemm_workspace_bytes(), dev)
+    ws = nv.workspace(256, dev)
+    A = {k: nv.NVFP4Tensor.empty(1, k, dev) for k in (H, I)}
+    for k, a in A.items():
+        nv.nvfp4_scale_quantize(torch.randn((1, k), device=dev).bfloat16(), a, ws, None, 1e-6, None)
+    for name, Kk in (("qkv", H), ("o", H), ("down", I)):
+        o = torch.empty((1, W[name].rows), dtype=torch.bfloat16, device=dev)
+        for rep in range(3):
+            flush.fill_(rep)
+            torch.cuda.synchronize()
+            assert L.nvfp4_debug_decode_trace_clear() == 0
+            nv.nvfp4_gemm(A[Kk], W[name], o, None, None, gws)
+            torch.cuda.synchronize()
+        buf = (ctypes.c_ulonglong * (256 * 16))()
+        assert L.nvfp4_debug_decode_trace(buf) == 0
+        t = np.array(buf, dtype=np.int64).reshape(256, 16)[:torch.cuda.get_device_properties(dev).multi_processor_count]
+        t0 = t[:, 0].min()
+        rec = {"gemm": name, "T": 1, "weight_MB": (W[name].codes.numel() + W[name].sf.numel()) / 1e6}
+        for k, n in enumerate(names):
+            col = (t[:, k][t[:, k] >= t0] - t0) / 1e3
+            rec[n] = {"med": round(float(np.median(col)), 2), "max": round(float(col.max()), 2)} if len(col) else None
+        for k, n in enumerate(stalls):
+            col = t[:, 8 + k] / 1e3
+            rec["stall_" + n] = {"med": round(float(np.median(col)), 2), "max": round(float(col.max()), 2)}
+        print(json.dumps(rec), flush=True)
+    assert nv.device_status() == 0
+
+
 # ----------------------------------------------------------- GPU (ours)
 def run_ours(args):
     import __graft_entry__
@@ -566,6 +652,9 @@ def run_ours(args):
     stream.synchronize()
     assert nv.device_status() == 0
 
+    if args.only == "decode_timeline":
+        decode_timeline(nv, W, dev)
+        return
     if args.only:
         # profiling target: launch one kernel of the step a few times, eagerly
         ev = {k: torch.cuda.Event(enable_timing=True) for k in PrefillBlock.EVENT_NAMES}
@@ -781,8 +870,10 @@ def main():
                     help="skip the side measurements (quantize at R=16384, GEMMs at T=1 and T=16384)")
     ap.add_argument("--no-configs", dest="configs", action="store_false",
                     help="skip the other workloads (single linear, decode MLP, T sweep, 8-layer long prefill)")
-    ap.add_argument("--only", choices=("swiglu", "down", "qkv", "norm_quantize", "step", "mma_probe"),
-                    help="profiling target: run one kernel of the step --only-reps times and exit")
+    ap.add_argument("--only", choices=("swiglu", "down", "qkv", "norm_quantize", "step", "mma_probe",
+                                       "decode_timeline"),
+                    help="profiling target: run one kernel of the step --only-reps times and exit "
+                         "(decode_timeline: the T=1 decode GEMMs' per-CTA timeline from a debug build)")
     ap.add_argument("--only-reps", type=int, default=3)
     args = ap.parse_args()
     assert args.warmup >= 3

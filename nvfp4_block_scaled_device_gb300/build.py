@@ -20,7 +20,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libnvfp4.so")
 SOURCES = ["api.cu", "quant.cu", "gemm.cu", "gemm2.cu", "gemv.cu", "gemm_decode.cu", "noalloc.cu", "probe.cu", "experts.cu"]
-HEADERS = ["common.cuh", "internal.h", "gemm_epilogue.cuh", "gemv.h"]
+HEADERS = ["common.cuh", "internal.h", "gemm_epilogue.cuh", "decode_epilogue.cuh", "gemv.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

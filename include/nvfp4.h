@@ -355,16 +355,23 @@ int nvfp4_mlp(const void* x, int64_t T, int64_t H, int64_t ldx,
  * Same computation, arguments, requirements and results as nvfp4_mlp, minus
  * the workspace: the intermediates live in a fixed 32 MiB array inside this
  * library (every GPU that loads the library holds it until the process
- * exits).  A call whose nvfp4_mlp_workspace_bytes(T, H, I, inter_mode)
- * exceeds 32 MiB returns NVFP4_ERR_WORKSPACE and enqueues nothing (at
- * H=5120, I=17408 that allows T up to about 2500 tokens with
- * NVFP4_INTER_STATIC and about 700 with NVFP4_INTER_DYNAMIC).
+ * exits).  The array must hold nvfp4_mlp's workspace without the split
+ * schedule's partial slots (those slots are used too when they also fit,
+ * which at H=5120, I=17408 and 152 SMs is up to T ~1070 with
+ * NVFP4_INTER_STATIC): a larger call returns NVFP4_ERR_WORKSPACE.  At
+ * H=5120, I=17408 the largest T is 2642 with NVFP4_INTER_STATIC and 704 with
+ * NVFP4_INTER_DYNAMIC.
+ *   - Argument errors (the statuses nvfp4_mlp returns) and
+ *     NVFP4_ERR_WORKSPACE are returned before anything is enqueued.
  *   - Allocates nothing and calls no allocator.  It enqueues one small
- *     cudaMemsetAsync that clears the array's amax words, then the
- *     nvfp4_mlp launches.
+ *     cudaMemsetAsync that clears the array's amax words and the split
+ *     schedule's flag words (a call that stopped early may have left them
+ *     non-zero), then the nvfp4_mlp launches.
  *   - The first call on a device looks up the array's device address (with
- *     that device current) and caches it; make that first call before any
- *     stream capture.
+ *     that device current) and caches it for the life of the process; make
+ *     that first call before any stream capture.  The cached address is not
+ *     looked up again: do not use the library across cudaDeviceReset or
+ *     anything else that destroys the device's primary context.
  *   - Every call shares the one array: calls that can overlap on the GPU
  *     (different streams, or several host threads) race with each other and
  *     must be serialised by the caller.
@@ -374,6 +381,15 @@ int nvfp4_mlp_noalloc(const void* x, int64_t T, int64_t H, int64_t ldx,
                       const nvfp4_tensor_t* W_gate, const nvfp4_tensor_t* W_up,
                       const nvfp4_tensor_t* W_down, int inter_mode, float* g_inter,
                       void* out, int64_t ldo, int add_residual, nvfp4_stream_t stream);
+
+/*
+ * nvfp4_noalloc_scratch -- diagnostics: the device address (on the current
+ * device) and the size of nvfp4_mlp_noalloc's fixed array.  The array
+ * belongs to nvfp4_mlp_noalloc; a caller may read it, or clear it between
+ * calls, but anything it writes there is overwritten or cleared by the next
+ * call.  Same caching as nvfp4_mlp_noalloc.
+ */
+int nvfp4_noalloc_scratch(void** device_ptr, size_t* bytes);
 
 #ifdef __cplusplus
 }

@@ -53,6 +53,7 @@ _SIGS = {
     "nvfp4_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "nvfp4_device_status": (ctypes.c_int, [ctypes.POINTER(ctypes.c_int), ctypes.c_int]),
     "nvfp4_mma_issue_rate": (ctypes.c_int, [ctypes.POINTER(ctypes.c_double)]),
+    "nvfp4_noalloc_scratch": (ctypes.c_int, [ctypes.POINTER(ctypes.c_void_p), ctypes.POINTER(ctypes.c_size_t)]),
     "nvfp4_experts_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
                                                         ctypes.c_int64]),
     "nvfp4_gemm_experts": (ctypes.c_int, [ctypes.POINTER(_TensorC), ctypes.POINTER(_TensorC), ctypes.c_int64,
@@ -289,6 +290,14 @@ def nvfp4_mlp_noalloc(x: torch.Tensor, norm_w: torch.Tensor, W_gate: NVFP4Tensor
     _check(lib().nvfp4_mlp_noalloc(_ptr(x), T, H, ldx, _ptr(norm_w), eps, ctypes.byref(wg), ctypes.byref(wu),
                                    ctypes.byref(wd), inter_mode, _ptr(g_inter), _ptr(out), ldo,
                                    int(bool(add_residual)), _stream(stream)), "nvfp4_mlp_noalloc")
+
+
+def noalloc_scratch():
+    """(device address, bytes) of nvfp4_mlp_noalloc's fixed array on the
+    current device (diagnostics and tests)."""
+    p, n = ctypes.c_void_p(0), ctypes.c_size_t(0)
+    _check(lib().nvfp4_noalloc_scratch(ctypes.byref(p), ctypes.byref(n)), "nvfp4_noalloc_scratch")
+    return int(p.value or 0), int(n.value)
 
 
 def nvfp4_mlp(x: torch.Tensor, norm_w: torch.Tensor, W_gate: NVFP4Tensor, W_up: NVFP4Tensor,

@@ -290,6 +290,29 @@ int run_linear(const nvfp4_tensor_t* A, const nvfp4_tensor_t* W, void* out, int6
 
 }  // namespace
 
+// Every argument check of nvfp4_mlp but the workspace's (nvfp4_mlp_noalloc
+// runs them before it touches its fixed array).
+int nvfp4::check_mlp_args(const void* x, int64_t T, int64_t H, int64_t ldx, const void* norm_w,
+                          const nvfp4_tensor_t* W_gate, const nvfp4_tensor_t* W_up, const nvfp4_tensor_t* W_down,
+                          int inter_mode, const float* g_inter, const void* out, int64_t ldo, int add_residual)
+{
+    NVFP4_TRY(check_bf16_matrix(x, T, H, ldx));
+    if (H % 64 != 0 || !norm_w) return NVFP4_ERR_INVALID_ARG;
+    if (!aligned(norm_w, 16)) return NVFP4_ERR_MISALIGNED;
+    NVFP4_TRY(check_tensor(W_gate));
+    NVFP4_TRY(check_tensor(W_up));
+    NVFP4_TRY(check_tensor(W_down));
+    const int64_t I = W_gate->rows;
+    if (W_gate->cols != H || W_up->cols != H || W_up->rows != I || W_down->rows != H || W_down->cols != I ||
+        I % 128 != 0)
+        return NVFP4_ERR_INVALID_ARG;
+    if (inter_mode != NVFP4_INTER_STATIC && inter_mode != NVFP4_INTER_DYNAMIC) return NVFP4_ERR_INVALID_ARG;
+    if (!g_inter) return NVFP4_ERR_INVALID_ARG;
+    NVFP4_TRY(check_bf16_matrix(out, T, H, ldo));
+    if (add_residual && out == x && ldo != ldx) return NVFP4_ERR_INVALID_ARG;
+    return NVFP4_OK;
+}
+
 // Workspace layouts (all offsets 256-B aligned).  Without the trailing
 // partial slots a call still runs, unsplit.
 //   swiglu: [256 amax words][split flags][DYNAMIC: bf16 T x I][partials]
@@ -568,20 +591,9 @@ int nvfp4_mlp(const void* x, int64_t T, int64_t H, int64_t ldx, const void* norm
               int inter_mode, float* g_inter, void* out, int64_t ldo, int add_residual, void* workspace,
               size_t workspace_bytes, nvfp4_stream_t stream)
 {
-    NVFP4_TRY(check_bf16_matrix(x, T, H, ldx));
-    if (H % 64 != 0 || !norm_w) return NVFP4_ERR_INVALID_ARG;
-    if (!aligned(norm_w, 16)) return NVFP4_ERR_MISALIGNED;
-    NVFP4_TRY(check_tensor(W_gate));
-    NVFP4_TRY(check_tensor(W_up));
-    NVFP4_TRY(check_tensor(W_down));
+    NVFP4_TRY(nvfp4::check_mlp_args(x, T, H, ldx, norm_w, W_gate, W_up, W_down, inter_mode, g_inter, out, ldo,
+                                    add_residual));
     const int64_t I = W_gate->rows;
-    if (W_gate->cols != H || W_up->cols != H || W_up->rows != I || W_down->rows != H || W_down->cols != I ||
-        I % 128 != 0)
-        return NVFP4_ERR_INVALID_ARG;
-    if (inter_mode != NVFP4_INTER_STATIC && inter_mode != NVFP4_INTER_DYNAMIC) return NVFP4_ERR_INVALID_ARG;
-    if (!g_inter) return NVFP4_ERR_INVALID_ARG;
-    NVFP4_TRY(check_bf16_matrix(out, T, H, ldo));
-    if (add_residual && out == x && ldo != ldx) return NVFP4_ERR_INVALID_ARG;
     const size_t base = mlp_base_workspace_bytes(T, H, I, inter_mode);
     if (!workspace || workspace_bytes < base) return NVFP4_ERR_WORKSPACE;
     if (!aligned(workspace, 256)) return NVFP4_ERR_MISALIGNED;

@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "nvfp4.h"
+
 namespace nvfp4 {
 
 // Block size of the row kernels (amax / quantize).  Both kernels reduce a
@@ -189,5 +191,11 @@ cudaError_t launch_gemm2(const CUtensorMap& map_a, const CUtensorMap& map_b0, co
 // public size helpers add the slots for the current device.
 size_t swiglu_base_workspace_bytes(int64_t T, int64_t I, int inter_mode);
 size_t mlp_base_workspace_bytes(int64_t T, int64_t H, int64_t I, int inter_mode);
+
+// nvfp4_mlp's argument checks, all but the workspace's: NVFP4_OK or the
+// status nvfp4_mlp returns for these arguments.
+int check_mlp_args(const void* x, int64_t T, int64_t H, int64_t ldx, const void* norm_w,
+                   const nvfp4_tensor_t* W_gate, const nvfp4_tensor_t* W_up, const nvfp4_tensor_t* W_down,
+                   int inter_mode, const float* g_inter, const void* out, int64_t ldo, int add_residual);
 
 }  // namespace nvfp4

@@ -46,13 +46,24 @@ int scratch_address(void** out)
 
 }  // namespace
 
+extern "C" int nvfp4_noalloc_scratch(void** device_ptr, size_t* bytes)
+{
+    if (!device_ptr || !bytes) return NVFP4_ERR_INVALID_ARG;
+    const int st = scratch_address(device_ptr);
+    if (st != NVFP4_OK) return st;
+    *bytes = kNoallocScratchBytes;
+    return NVFP4_OK;
+}
+
 extern "C" int nvfp4_mlp_noalloc(const void* x, int64_t T, int64_t H, int64_t ldx, const void* norm_w, float eps,
                                  const nvfp4_tensor_t* W_gate, const nvfp4_tensor_t* W_up,
                                  const nvfp4_tensor_t* W_down, int inter_mode, float* g_inter, void* out,
                                  int64_t ldo, int add_residual, nvfp4_stream_t stream)
 {
-    if (!W_gate || T < 1) return NVFP4_ERR_INVALID_ARG;
-    if (inter_mode != NVFP4_INTER_STATIC && inter_mode != NVFP4_INTER_DYNAMIC) return NVFP4_ERR_INVALID_ARG;
+    // every argument error is returned before anything is enqueued
+    const int arg = nvfp4::check_mlp_args(x, T, H, ldx, norm_w, W_gate, W_up, W_down, inter_mode, g_inter, out, ldo,
+                                          add_residual);
+    if (arg != NVFP4_OK) return arg;
     // the intermediates of this call must fit the fixed array (the split
     // schedule's partial slots are used when they fit as well)
     if (nvfp4::mlp_base_workspace_bytes(T, H, W_gate->rows, inter_mode) > kNoallocScratchBytes)
@@ -61,9 +72,9 @@ extern "C" int nvfp4_mlp_noalloc(const void* x, int64_t T, int64_t H, int64_t ld
     const int st = scratch_address(&scratch);
     if (st != NVFP4_OK) return st;
     // The array keeps whatever the previous call left.  The amax words and
-    // the split schedule's ready flags at its start must be zero when a call
-    // begins (a completed call leaves them zero; a call that stopped early
-    // might not), so clear them first.
+    // the split schedule's ready flags and tickets at its start must be zero
+    // when a call begins (a completed call leaves them zero; a call that
+    // stopped early might not), so clear them first.
     if (cudaMemsetAsync(scratch, 0, 256 + nvfp4::kSplitFlagBytes, (cudaStream_t)stream) != cudaSuccess)
         return NVFP4_ERR_CUDA;
     return nvfp4_mlp(x, T, H, ldx, norm_w, eps, W_gate, W_up, W_down, inter_mode, g_inter, out, ldo, add_residual,

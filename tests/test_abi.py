@@ -131,3 +131,31 @@ def test_experts_arguments_rejected_on_host(L):
     b = nv.experts_workspace_bytes(16, 2, 256, 4)
     assert b >= (32 + 127 * 4) // 128 * 128 * (128 + 16)
     assert nv.experts_workspace_bytes(0, 2, 256, 4) == 0
+
+
+def test_noalloc_argument_errors_before_any_cuda_call(L):
+    """nvfp4_mlp_noalloc returns nvfp4_mlp's argument statuses, and refuses an
+    oversized request, before it looks up or clears its fixed array (no CUDA
+    call: these run on a machine without a GPU)."""
+    import nvfp4_block_scaled_device_gb300 as nv
+    NULL = None
+    H, I = 256, 512
+    g = nv._TensorC(16, 256, 4, I, H, H // 2)      # gate / up [I x H]
+    d = nv._TensorC(16, 256, 4, H, I, I // 2)      # down [H x I]
+    call = lambda x, T, wg, wu, wd, mode, gi, out: L.nvfp4_mlp_noalloc(
+        x, T, H, H, 16, 1e-6, ctypes.byref(wg), ctypes.byref(wu) if wu is not None else NULL, ctypes.byref(wd),
+        mode, gi, out, H, 1, NULL)
+    assert call(16, 4, g, None, d, 0, 16, 16) == 1           # missing W_up
+    assert call(16, 4, g, g, d, 7, 16, 16) == 1              # bad intermediate-scale mode
+    assert call(16, 4, g, g, d, 0, NULL, 16) == 1            # missing g_inter
+    assert call(18, 4, g, g, d, 0, 16, 16) == 2              # misaligned x
+    bad = nv._TensorC(16, 256, 4, I, H + 64, (H + 64) // 2)
+    assert call(16, 4, bad, bad, d, 0, 16, 16) == 1          # gate cols != H
+    # larger than the fixed array (valid arguments otherwise): NVFP4_ERR_WORKSPACE
+    Hb, Ib = 5120, 17408
+    gb = nv._TensorC(16, 256, 4, Ib, Hb, Hb // 2)
+    db = nv._TensorC(16, 256, 4, Hb, Ib, Ib // 2)
+    st = L.nvfp4_mlp_noalloc(16, 705, Hb, Hb, 16, 1e-6, ctypes.byref(gb), ctypes.byref(gb), ctypes.byref(db),
+                             nv.NVFP4_INTER_DYNAMIC, 16, 16, Hb, 1, NULL)
+    assert st == 5
+    assert L.nvfp4_noalloc_scratch(NULL, NULL) == 1

@@ -6,7 +6,11 @@ live in a fixed array inside the library instead of a caller workspace.
 Checked through the C ABI against nvfp4_mlp (which takes a workspace) on the
 same inputs, within the MLP tolerance of the other tests, on two calls in a
 row (the array keeps the previous call's contents), in both intermediate-
-scale modes; and a request larger than the array is refused without work.
+scale modes; after the array's amax and flag words were left dirty, as a
+call that stopped early may leave them, at full size with the GEMMs using
+the array's split-schedule slots (T=1: the tensor-core decode GEMMs' tickets
+and partials; T=512: the down projection's split schedule); and a request
+larger than the array is refused without work.
 This file sorts last so a stop-at-first-failure run has run everything else.
 """
 import ctypes
@@ -61,6 +65,45 @@ def test_noalloc_matches_workspace_mlp(nv, T, H, I, mode):
         assert torch.isfinite(out.float()).all(), call
         close(out, ref)
         assert g.item() == g_ref.item()
+
+
+class _DeviceBytes:
+    """A torch view of device bytes at a raw address (CUDA array interface)."""
+
+    def __init__(self, addr, n):
+        self.__cuda_array_interface__ = {"shape": (n,), "typestr": "|u1", "data": (addr, False), "version": 3}
+
+
+@pytest.mark.parametrize("T", [1, 512])
+def test_noalloc_recovers_dirty_words_and_uses_split_slots(nv, T):
+    H, I = 5120, 17408
+    rng = np.random.default_rng(900 + T)
+    ws = nv.workspace(256)
+    x = dev(synthetic.normal(rng, (T, H)))
+    nw = dev(synthetic.normal(rng, (H,), mean=1.0, std=0.05))
+    Wg = quantize_gpu(synthetic.normal(rng, (I, H), std=0.02), ws)
+    Wu = quantize_gpu(synthetic.normal(rng, (I, H), std=0.02), ws)
+    Wd = quantize_gpu(synthetic.normal(rng, (H, I), std=0.02), ws)
+    g_ref = torch.full((1,), 0.004, dtype=torch.float32, device="cuda")
+    ref = torch.empty_like(x)
+    mode = nv.NVFP4_INTER_STATIC
+    nv.nvfp4_mlp(x, nw, Wg, Wu, Wd, mode, g_ref, ref, nv.workspace(nv.mlp_workspace_bytes(T, H, I, mode)))
+    # the split slots fit in the array next to the intermediates
+    addr, n = nv.noalloc_scratch()
+    assert addr != 0 and n == 32 << 20
+    base = nv.mlp_workspace_bytes(T, H, I, mode) - (nv.gemm_workspace_bytes() - 8192)
+    assert base + (nv.gemm_workspace_bytes() - 8192) <= n
+    words = torch.as_tensor(_DeviceBytes(addr, 256 + 8192), device="cuda")
+    for call in range(2):
+        words.fill_(0xA5)              # amax words, flags and tickets left dirty
+        out = torch.full_like(x, float("nan"))
+        g = torch.full((1,), 0.004, dtype=torch.float32, device="cuda")
+        nv.nvfp4_mlp_noalloc(x, nw, Wg, Wu, Wd, mode, g, out)
+        torch.cuda.synchronize()
+        assert nv.device_status() == 0
+        assert torch.isfinite(out.float()).all(), call
+        close(out, ref)
+        assert int(words[256:].count_nonzero()) == 0      # the call leaves its flag words zero
 
 
 def test_noalloc_refuses_requests_beyond_the_array(nv):

@@ -76,6 +76,14 @@ def test_rope_layouts(nv, ws, T, N, K, col0, heads, hd, rd):
 
 
 def test_rope_split_schedule(nv, ws):
-    """A deep-K shape that takes the split schedule (partials combined
-    before the epilogue)."""
+    """A deep-K shape given the split workspace: at T=3 the tensor-core decode
+    kernel, split along K over all SMs, its partials combined before the
+    rotating epilogue."""
     run(nv, ws, 3, 1024, 16384, 0, 8, 128, 64, False, seed=99, split=True)
+
+
+@pytest.mark.parametrize("T", [1, 8])
+def test_rope_qkv_decode_tensor_cores(nv, ws, T):
+    """The QKV projection at decode sizes with the split workspace (the
+    tensor-core decode kernel's epilogue rotates)."""
+    run(nv, ws, T, 7168, 5120, 0, 48, 128, 64, False, seed=40 + T, split=True)

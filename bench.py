@@ -613,6 +613,34 @@ def decode_timeline(nv, W, dev):
     assert nv.device_status() == 0
 
 
+def row_kernel_only(nv, dev, norm, reps):
+    """Profiling target: the one-launch scale + quantize (with the RMSNorm
+    when norm) at R=16384 x K=5120, `reps` launches on one stream after one
+    untimed launch; prints the mean launch time from CUDA events (a time
+    taken under a profiler is not a measurement)."""
+    R, K = 16384, H
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(7)
+    x = torch.randn((R, K), generator=gen, device=dev).bfloat16()
+    w = (1 + 0.05 * torch.randn((K,), generator=gen, device=dev)).bfloat16() if norm else None
+    t = nv.NVFP4Tensor.empty(R, K, dev)
+    ws = nv.workspace(256, dev)
+    stream = torch.cuda.Stream(dev)
+    with torch.cuda.stream(stream):
+        nv.nvfp4_scale_quantize(x, t, ws, w, 1e-6, stream)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            nv.nvfp4_scale_quantize(x, t, ws, w, 1e-6, stream)
+        e1.record(stream)
+    stream.synchronize()
+    assert nv.device_status() == 0
+    us = e0.elapsed_time(e1) / reps * 1e3
+    alg = 2 * R * K + 0.5625 * R * K
+    log(f"[bench] scale_quantize R={R} K={K} norm={norm}: {us:.1f} us per launch, {alg / us / 1e3:.0f} GB/s "
+        f"(algorithmic bytes), {reps} launches")
+
+
 # ----------------------------------------------------------- GPU (ours)
 def run_ours(args):
     import __graft_entry__
@@ -630,6 +658,9 @@ def run_ours(args):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
     T = args.T
+    if args.only in ("quantize_R16384", "norm_quantize_R16384"):
+        row_kernel_only(nv, dev, args.only.startswith("norm"), args.only_reps)
+        return
 
     t_in = time.perf_counter()
     wbits, x_bits = make_inputs(T)
@@ -871,7 +902,7 @@ def main():
     ap.add_argument("--no-configs", dest="configs", action="store_false",
                     help="skip the other workloads (single linear, decode MLP, T sweep, 8-layer long prefill)")
     ap.add_argument("--only", choices=("swiglu", "down", "qkv", "norm_quantize", "step", "mma_probe",
-                                       "decode_timeline"),
+                                       "decode_timeline", "quantize_R16384", "norm_quantize_R16384"),
                     help="profiling target: run one kernel of the step --only-reps times and exit "
                          "(decode_timeline: the T=1 decode GEMMs' per-CTA timeline from a debug build)")
     ap.add_argument("--only-reps", type=int, default=3)

@@ -176,11 +176,14 @@ def test_deterministic(nv, ws):
 
 
 # One-launch scale + quantize (cooperative kernel with a grid barrier).  The
-# shapes cover the resident variant (every row pair its own block, rows held
-# in registers) and the looping variant (more rows than resident blocks, or
-# rows wider than the register share), with and without the RMSNorm.
+# shapes cover the resident variant (every row held in registers by one
+# block) and the looping variant (more rows than resident blocks hold, or
+# rows wider than the register share), with and without the RMSNorm, up to
+# the 16384 x 5120 input that the row-kernel bandwidth figure is taken on.
 FUSED = [(1, 64, False), (3, 128, True), (17, 320, False), (130, 1024, True), (777, 5120, True),
-         (1024, 5120, True), (1024, 5120, False), (1300, 5120, True), (5, 17408, True), (2500, 256, False)]
+         (1024, 5120, True), (1024, 5120, False), (1300, 5120, True), (5, 17408, True), (2500, 256, False),
+         (4000, 5120, True), (4000, 5120, False), (6000, 256, True), (6000, 256, False), (1000, 17408, True),
+         (16384, 5120, True), (16384, 5120, False), (20, 28672, True), (20, 32768, False)]
 
 
 @pytest.mark.parametrize("rows,cols,norm", FUSED)

@@ -699,6 +699,8 @@ def run_ours(args):
                     nv.nvfp4_gemm(blk.s, W["down"], out, blk.x1, stream, blk.ws_gemm)
                 elif args.only == "qkv":
                     nv.nvfp4_gemm(blk.h, W["qkv"], blk.qkv, None, stream, blk.ws_gemm)
+                elif args.only == "o":
+                    nv.nvfp4_gemm(blk.a, W["o"], blk.x1, x, stream, blk.ws_gemm)
                 elif args.only == "norm_quantize":
                     nv.nvfp4_scale_quantize(x, blk.h, blk.ws_amax, blk.attn_norm, 1e-6, stream)
                 elif args.only == "step":
@@ -901,7 +903,7 @@ def main():
                     help="skip the side measurements (quantize at R=16384, GEMMs at T=1 and T=16384)")
     ap.add_argument("--no-configs", dest="configs", action="store_false",
                     help="skip the other workloads (single linear, decode MLP, T sweep, 8-layer long prefill)")
-    ap.add_argument("--only", choices=("swiglu", "down", "qkv", "norm_quantize", "step", "mma_probe",
+    ap.add_argument("--only", choices=("swiglu", "down", "qkv", "o", "norm_quantize", "step", "mma_probe",
                                        "decode_timeline", "quantize_R16384", "norm_quantize_R16384"),
                     help="profiling target: run one kernel of the step --only-reps times and exit "
                          "(decode_timeline: the T=1 decode GEMMs' per-CTA timeline from a debug build)")

@@ -734,6 +734,27 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
     return a | (b << 16);
 }
 
+// Two binary32 values -> bf16x2, each rounded to nearest even (lo in the
+// low half): pack_bf16x2 in one instruction.
+__device__ __forceinline__ uint32_t cvt_bf16x2(float lo, float hi)
+{
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// Sum of two bf16x2, each half rounded to nearest even once.  For bf16
+// operands this equals rounding their binary32 sum to bf16: that sum is
+// exact when the exponents differ by at most 15, and otherwise the smaller
+// operand lies far below half an ulp of the larger, which both roundings
+// then return.
+__device__ __forceinline__ uint32_t add_bf16x2(uint32_t a, uint32_t b)
+{
+    uint32_t r;
+    asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
 // Byte offset of scale (row r, scale column c) in the 128x4-tile layout.
 __device__ __forceinline__ int64_t sf_offset(int64_t r, int64_t c, int64_t kb_pad)
 {

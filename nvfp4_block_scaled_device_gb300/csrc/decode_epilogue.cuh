@@ -42,18 +42,20 @@ __device__ __forceinline__ void decode_epilogue(const GemmArgs& args, const EpiS
         for (int t = tid; t < M * pairs; t += kNT) {
             const int m = t / pairs, r = 2 * (t % pairs);
             const int64_t n = n0 + r;
-            float y0 = bf16_round(__fmul_rn(racc[r * M + m], alpha0));
-            float y1 = bf16_round(__fmul_rn(racc[(r + 1) * M + m], alpha0));
+            uint32_t o;
             if (args.rope_pos) {
+                // rotated in binary32 from the rounded values (no residual)
+                float y0 = bf16_round(__fmul_rn(racc[r * M + m], alpha0));
+                float y1 = bf16_round(__fmul_rn(racc[(r + 1) * M + m], alpha0));
                 RopeCursor rk = rope_begin(args, m, n);
                 rope_step(args, rk, y0, y1);
+                o = pack_bf16x2(y0, y1);
+            } else {
+                o = cvt_bf16x2(__fmul_rn(racc[r * M + m], alpha0), __fmul_rn(racc[(r + 1) * M + m], alpha0));
+                if (args.residual)
+                    o = add_bf16x2(*reinterpret_cast<const uint32_t*>(args.residual + m * args.ldr + n), o);
             }
-            if (args.residual) {
-                const uint32_t q = *reinterpret_cast<const uint32_t*>(args.residual + m * args.ldr + n);
-                y0 = __fadd_rn(bf16_lo(q), y0);
-                y1 = __fadd_rn(bf16_hi(q), y1);
-            }
-            *reinterpret_cast<uint32_t*>(args.out + m * args.ldo + n) = pack_bf16x2(y0, y1);
+            *reinterpret_cast<uint32_t*>(args.out + m * args.ldo + n) = o;
         }
         return;
     }

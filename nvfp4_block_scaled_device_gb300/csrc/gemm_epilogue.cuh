@@ -124,29 +124,33 @@ __device__ __forceinline__ void epilogue_row(const GemmArgs& args, bool swiglu, 
                 for (int t = 0; t < 4; t++) {
                     const int j = jb + 8 * t;
                     const int64_t n = n_base + j;
-                    float y[8];
-#pragma unroll
-                    for (int i = 0; i < 8; i++) y[i] = bf16_round(__fmul_rn(v[j + i], alpha0));
+                    uint4 o;
                     if (kRope) {
+                        // rotated in binary32 from the rounded values, then
+                        // rounded (the rotation has no residual)
+                        float y[8];
+#pragma unroll
+                        for (int i = 0; i < 8; i++) y[i] = bf16_round(__fmul_rn(v[j + i], alpha0));
 #pragma unroll
                         for (int q = 0; q < 4; q++) rope_step(args, rk, y[2 * q], y[2 * q + 1]);
-                    }
-                    if (n < args.N) {
-                        if (rrow) {
-                            y[0] = __fadd_rn(bf16_lo(rp[t].x), y[0]);
-                            y[1] = __fadd_rn(bf16_hi(rp[t].x), y[1]);
-                            y[2] = __fadd_rn(bf16_lo(rp[t].y), y[2]);
-                            y[3] = __fadd_rn(bf16_hi(rp[t].y), y[3]);
-                            y[4] = __fadd_rn(bf16_lo(rp[t].z), y[4]);
-                            y[5] = __fadd_rn(bf16_hi(rp[t].z), y[5]);
-                            y[6] = __fadd_rn(bf16_lo(rp[t].w), y[6]);
-                            y[7] = __fadd_rn(bf16_hi(rp[t].w), y[7]);
-                        }
-                        uint4 o;
                         o.x = pack_bf16x2(y[0], y[1]);
                         o.y = pack_bf16x2(y[2], y[3]);
                         o.z = pack_bf16x2(y[4], y[5]);
                         o.w = pack_bf16x2(y[6], y[7]);
+                    } else {
+                        o.x = cvt_bf16x2(__fmul_rn(v[j], alpha0), __fmul_rn(v[j + 1], alpha0));
+                        o.y = cvt_bf16x2(__fmul_rn(v[j + 2], alpha0), __fmul_rn(v[j + 3], alpha0));
+                        o.z = cvt_bf16x2(__fmul_rn(v[j + 4], alpha0), __fmul_rn(v[j + 5], alpha0));
+                        o.w = cvt_bf16x2(__fmul_rn(v[j + 6], alpha0), __fmul_rn(v[j + 7], alpha0));
+                    }
+                    if (n < args.N) {
+                        if (rrow) {
+                            // out = bf16(residual + bf16(alpha * acc))
+                            o.x = add_bf16x2(rp[t].x, o.x);
+                            o.y = add_bf16x2(rp[t].y, o.y);
+                            o.z = add_bf16x2(rp[t].z, o.z);
+                            o.w = add_bf16x2(rp[t].w, o.w);
+                        }
                         *reinterpret_cast<uint4*>(orow + n) = o;
                     }
                 }
@@ -166,9 +170,7 @@ __device__ __forceinline__ void epilogue_row(const GemmArgs& args, bool swiglu, 
             }
         } else {
 #pragma unroll
-            for (int i = 0; i < 64; i++)
-                pk[i] = pack_bf16x2(bf16_round(__fmul_rn(v[2 * i], alpha0)),
-                                    bf16_round(__fmul_rn(v[2 * i + 1], alpha0)));
+            for (int i = 0; i < 64; i++) pk[i] = cvt_bf16x2(__fmul_rn(v[2 * i], alpha0), __fmul_rn(v[2 * i + 1], alpha0));
         }
         const int lane = threadIdx.x & 31;
         const int64_t row0 = row - lane;                 // the warp's first row
@@ -212,10 +214,10 @@ __device__ __forceinline__ void epilogue_row(const GemmArgs& args, bool swiglu, 
                     if (args.residual) {
                         // out = bf16(residual + t)
                         const uint4 q = rp[slot];
-                        o.x = pack_bf16x2(__fadd_rn(bf16_lo(q.x), bf16_lo(t.x)), __fadd_rn(bf16_hi(q.x), bf16_hi(t.x)));
-                        o.y = pack_bf16x2(__fadd_rn(bf16_lo(q.y), bf16_lo(t.y)), __fadd_rn(bf16_hi(q.y), bf16_hi(t.y)));
-                        o.z = pack_bf16x2(__fadd_rn(bf16_lo(q.z), bf16_lo(t.z)), __fadd_rn(bf16_hi(q.z), bf16_hi(t.z)));
-                        o.w = pack_bf16x2(__fadd_rn(bf16_lo(q.w), bf16_lo(t.w)), __fadd_rn(bf16_hi(q.w), bf16_hi(t.w)));
+                        o.x = add_bf16x2(q.x, t.x);
+                        o.y = add_bf16x2(q.y, t.y);
+                        o.z = add_bf16x2(q.z, t.z);
+                        o.w = add_bf16x2(q.w, t.w);
                     }
                     *reinterpret_cast<uint4*>(args.out + orow * args.ldo + n) = o;
                 }

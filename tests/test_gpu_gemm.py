@@ -247,3 +247,35 @@ def test_pair_split_sampled(nv, ws, M, N, K):
     alpha = float(np.float32(np.float32(ga) * np.float32(gw)))
     got = f64(host(o1))[m, n]
     check_close(got, alpha * dot + f64(r)[m, n], alpha * adot, f"{M}x{N}x{K} pair split sampled")
+
+
+# The residual epilogue, bit for bit: with a residual r the output is
+# bf16_RNE(float(r) + float(y)), y the same GEMM's output without one
+# (R8's residual step).  y comes from the kernel itself, so the check pins
+# the epilogue's arithmetic exactly on every path that has one: the 1-SM
+# kernel with whole tiles and with two tiles on some CTAs (its staged
+# stores), the pair kernel's whole tiles (80 tiles on 76 pairs: staged
+# stores on the four pairs with two tiles, direct stores on the last
+# tiles), the split schedule, and the decode kernels.
+EPI_CASES = [(33, 512, 256, False), (100, 40960, 256, False), (1024, 5120, 5120, False),
+             (1024, 5120, 17408, True), (4, 5120, 5120, True), (1, 5120, 5120, False)]
+
+
+@pytest.mark.parametrize("M,N,K,with_ws", EPI_CASES)
+def test_residual_epilogue_bit_exact(nv, ws, M, N, K, with_ws):
+    g = torch.Generator(device="cuda")
+    g.manual_seed(M + N + K)
+    A = nv.quantize_new(torch.randn((M, K), generator=g, device="cuda").bfloat16(), ws)
+    W = nv.quantize_new((0.02 * torch.randn((N, K), generator=g, device="cuda")).bfloat16(), ws)
+    r = torch.randn((M, N), generator=g, device="cuda").bfloat16()
+    gws = nv.workspace(nv.gemm_workspace_bytes()) if with_ws else None
+    y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    out = torch.empty_like(y)
+    nv.nvfp4_gemm(A, W, y, workspace=gws)
+    nv.nvfp4_gemm(A, W, out, residual=r, workspace=gws)
+    torch.cuda.synchronize()
+    assert nv.device_status() == 0
+    want = (r.float().cpu() + y.float().cpu()).bfloat16()
+    got = out.cpu()
+    bad = (got.view(torch.int16) != want.view(torch.int16)).sum().item()
+    assert bad == 0, f"{M}x{N}x{K}: {bad} outputs differ from bf16(r + y)"

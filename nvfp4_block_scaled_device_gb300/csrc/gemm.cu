@@ -648,10 +648,11 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     args.sk_flags[c * kSplitFlagsPerCta + we] = 0;
                 if (warp == kEpiWarp0 && lane == 0) TRACE(1216, ecount - 1);
             }
-            // bf16 stores through the staging while later tiles accumulate;
-            // direct stores (lower latency) for the exposed last epilogue
-            // and in the split kernel (deep K: few, long segments)
-            const bool last = sched.next >= sched.tiles;   // whole tiles: no tile follows
+            // bf16 stores through the shared-memory staging (whole 256-byte
+            // row segments per warp store); with few rows (a tile of at most
+            // 64) the thread of each row stores it directly, which costs less
+            // than the staging's rounds
+            const uint32_t stage_arg = args.M > 64 ? epi_stage : 0u;
             if (kGrouped) {
                 // the tile's expert scale; the A row's output row (padding
                 // rows go past the last output row: not stored); each row
@@ -663,8 +664,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 epilogue_row<false>(gargs, false, v, orow >= 0 ? (int64_t)orow : args.grp_out_rows, nt, h, alpha_e, alpha_e,
                              1.0f, wamax, 0u);
             } else {
-                epilogue_row<kRope>(args, swiglu, v, row, nt, h, alpha0, alpha1, g_inter, wamax,
-                             (!kSplit && !last) ? epi_stage : 0u);
+                epilogue_row<kRope>(args, swiglu, v, row, nt, h, alpha0, alpha1, g_inter, wamax, stage_arg);
             }
             if (warp == kEpiWarp0 && lane == 0 && ecount == 1) TRACE_CTA(2);
             if (warp == kEpiWarp0 && lane == 0) TRACE_CTA(3);

@@ -39,7 +39,8 @@ constexpr int kSfbBytes = 8 * kSfTile;         // both 128-row halves of B, 4 K-
 constexpr int kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;  // 38912
 constexpr int kCtrlBytes = 256;
 // ring, control block, the epilogue warps' bf16 staging areas, alignment slack
-constexpr int kSmemBytes = kStages * kStageBytes + kCtrlBytes + 8 * kEpiStageBytes + 1024;   // 8 epilogue warps
+constexpr int kEpiRows = 8;                            // bf16 staging rows per epilogue warp
+constexpr int kSmemBytes = kStages * kStageBytes + kCtrlBytes + 8 * epi_stage_bytes(kEpiRows) + 1024;   // 8 epilogue warps
 static_assert(kSmemBytes <= 232448, "shared memory per block");
 static_assert(kStageBytes % 1024 == 0, "stages keep 1024-byte alignment (128-byte swizzle atoms)");
 
@@ -479,7 +480,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
         const int h = (warp - kEpiWarp0) >> 2;   // which half of the tile's columns
         // this warp's bf16 staging area, after the ring and the control block
         const uint32_t epi_stage = base + (uint32_t)(kStages * kStageBytes + kCtrlBytes) +
-                                   (uint32_t)((warp - kEpiWarp0) * kEpiStageBytes);
+                                   (uint32_t)((warp - kEpiWarp0) * epi_stage_bytes(kEpiRows));
         const uint32_t lane_addr = tmem + ((uint32_t)(q * 32) << 16);
         const uint32_t acc_empty_leader = map_to_cta(smem_u32(&ctrl->acc_empty), 0);
         const float ga = *args.ga;
@@ -568,11 +569,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
                 for (int64_t c = pair + 1 + lane; c < p_end; c += 32)
                     args.sk_flags[(2 * c + rank) * kSplitFlagsPerCta + we] = 0;
             }
-            // staged bf16 stores while later tiles accumulate; direct stores
-            // for the exposed last epilogue and in the split kernel
-            const bool last = sched.next >= sched.tiles;   // whole tiles: no tile follows
-            epilogue_row<kRope>(args, swiglu, v, row, nt, h, alpha0, alpha1, g_inter, wamax,
-                         (!kSplit && !last) ? epi_stage : 0u);
+            // bf16 stores staged through shared memory: whole 256-byte row
+            // segments per warp store
+            epilogue_row<kRope, kEpiRows>(args, swiglu, v, row, nt, h, alpha0, alpha1, g_inter, wamax, epi_stage);
         }
         if (args.epilogue == kEpiSwigluBf16) {
 #pragma unroll

@@ -67,13 +67,13 @@ __device__ __forceinline__ void rope_step(const GemmArgs& a, RopeCursor& k, floa
 }
 
 // bf16 output rows can go out through a per-warp shared-memory staging area
-// of kEpiStageRows rows: a thread holds one row's 128 columns, so storing
-// them straight from registers makes every warp store touch 32 rows, which
-// slows the loads of the tiles accumulating meanwhile; staged, each warp
-// store writes two whole 256-byte row segments.
-constexpr int kEpiStageRows = 4;
-constexpr int kEpiStageRowBytes = 256 + 16;            // padded: the 4 rows' 16-byte chunks hit distinct banks
-constexpr int kEpiStageBytes = kEpiStageRows * kEpiStageRowBytes;   // per epilogue warp
+// of kStageRows rows (4 or 8, as the kernel's shared memory allows): a thread
+// holds one row's 128 columns, so storing them straight from registers makes
+// every warp store touch 32 rows; staged, each warp store writes two whole
+// 256-byte row segments.
+constexpr int kEpiStageRowBytes = 256 + 16;            // padded: the staged rows' 16-byte chunks hit distinct banks
+__host__ __device__ constexpr int epi_stage_bytes(int stage_rows) { return stage_rows * kEpiStageRowBytes; }   // per epilogue warp
+constexpr int kEpiStageBytes = epi_stage_bytes(4);
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, const uint4& v)
 {
@@ -91,12 +91,12 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr)
 
 // v: this thread's accumulator values; row: its output row (warp-converged
 // call: every lane of the warp, rows >= M included); stage: this warp's
-// kEpiStageBytes of shared memory (shared-space address), or 0 for the
-// direct bf16 stores (lower latency: for an epilogue nothing overlaps).
+// epi_stage_bytes(kStageRows) of shared memory (shared-space address), or 0
+// for the direct bf16 stores (fewer steps: for a tile of few rows).
 // kRope: the rotary embedding of the bf16 output (args.rope_*) is compiled
 // in; the kernels run that instantiation only for a call that asks for it,
 // so the others carry none of its code or registers.
-template <bool kRope>
+template <bool kRope, int kStageRows = 4>
 __device__ __forceinline__ void epilogue_row(const GemmArgs& args, bool swiglu, float (&v)[128], int64_t row,
                                              int64_t nt, int h, float alpha0, float alpha1, float g_inter,
                                              float& wamax, uint32_t stage)
@@ -176,15 +176,16 @@ __device__ __forceinline__ void epilogue_row(const GemmArgs& args, bool swiglu, 
         const int64_t row0 = row - lane;                 // the warp's first row
         const int c = lane & 15;                         // 16-byte chunk (8 columns) of a staged row
         const int64_t n = n_base + 8 * c;
-        constexpr int kRounds = 32 / kEpiStageRows;
-        constexpr int kPerRound = kEpiStageRows / 2;      // chunks a lane stores per round
-        constexpr int kAhead = 3;                          // rounds of residual loads in flight
+        static_assert(kStageRows == 4 || kStageRows == 8, "staging rows");
+        constexpr int kRounds = 32 / kStageRows;
+        constexpr int kPerRound = kStageRows / 2;         // chunks a lane stores per round
+        constexpr int kAhead = kStageRows == 4 ? 3 : 1;   // rounds of residual loads in flight
         // this lane's output chunk (round r, part hh): row
-        // row0 + kEpiStageRows * r + 2 * hh + lane / 16, columns n .. n + 7.
+        // row0 + kStageRows * r + 2 * hh + lane / 16, columns n .. n + 7.
         // Residual loads run kAhead rounds ahead of the stores (an output
         // aliasing the residual element for element is read by the thread
         // that later overwrites it, before it does).
-        auto chunk_row = [&](int r, int hh) { return row0 + kEpiStageRows * r + 2 * hh + (lane >> 4); };
+        auto chunk_row = [&](int r, int hh) { return row0 + kStageRows * r + 2 * hh + (lane >> 4); };
         auto load_res = [&](int r, int hh) {
             const int64_t orow = chunk_row(r, hh);
             return (args.residual && orow < args.M && n < args.N)
@@ -196,8 +197,8 @@ __device__ __forceinline__ void epilogue_row(const GemmArgs& args, bool swiglu, 
         for (int i = 0; i < kAhead * kPerRound; i++) rp[i] = load_res(i / kPerRound, i % kPerRound);
 #pragma unroll
         for (int r = 0; r < kRounds; r++) {
-            if ((lane / kEpiStageRows) == r) {
-                const uint32_t dst = stage + (uint32_t)(lane % kEpiStageRows) * kEpiStageRowBytes;
+            if ((lane / kStageRows) == r) {
+                const uint32_t dst = stage + (uint32_t)(lane % kStageRows) * kEpiStageRowBytes;
 #pragma unroll
                 for (int j = 0; j < 16; j++)
                     st_shared_v4(dst + 16u * j, make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]));

@@ -113,6 +113,8 @@ struct Ctrl {
     uint64_t teardown;
     uint32_t tmem_base;
     int abort_flag;
+    int fix_arrive;       // split fix-up: arrivals of the epilogue warps (epi_sync)
+    uint64_t fix_full;    // split fix-up: the contributors' partial rows landed in the ring
 };
 static_assert(sizeof(Ctrl) <= kCtrlBytes, "control block");
 
@@ -198,6 +200,37 @@ __device__ __forceinline__ int flag_get_relaxed(const int* f)
 // or none when f is null, and a vote decides); gives up like mbar_wait_warp.
 // The polls are relaxed: the caller orders its reads of the flagged data
 // after the wait with one acquire fence.
+// Bounded barrier of the kEpiWarps epilogue warps (warp-converged calls):
+// each warp arrives on a shared-memory counter and waits until it reaches
+// target (kEpiWarps for a first barrier, 2 kEpiWarps for a second one);
+// memory before the arrival is visible to every warp after the wait.  A warp
+// gives up when the CTA's abort flag is raised or after the time limit (then
+// recording a timeout and raising the flag itself); returns false then.
+__device__ __forceinline__ bool epi_sync(int* counter, int target, volatile int* abort_flag, int* status, int site)
+{
+    int ok = 1;
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) {
+        __threadfence_block();
+        atomicAdd(counter, 1);
+        const uint64_t t0 = clock64();
+        while (*reinterpret_cast<volatile int*>(counter) < target) {
+            if (*abort_flag) {
+                ok = 0;
+                break;
+            }
+            if ((uint64_t)(clock64() - t0) > kWaitLimitCycles) {
+                *abort_flag = 1;
+                if (status) atomicCAS(status, 0, kErrTimeout * 100 + site);
+                ok = 0;
+                break;
+            }
+        }
+        __threadfence_block();
+    }
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
 __device__ __forceinline__ bool flag_wait_warp(const int* f, volatile int* abort_flag, int* status, int site)
 {
     const uint64_t t0 = clock64();
@@ -263,7 +296,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         mbar_init(smem_u32(&ctrl->acc_full), 1);
         mbar_init(smem_u32(&ctrl->acc_empty), kEpiWarps);
         mbar_init(smem_u32(&ctrl->teardown), 1);
+        mbar_init(smem_u32(&ctrl->fix_full), kEpiWarps);
         ctrl->abort_flag = 0;
+        ctrl->fix_arrive = 0;
         fence_barrier_init();
     }
     if (warp == 0 && lane == 0) {
@@ -579,11 +614,69 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 #ifdef NVFP4_TRACE
                 if (blockIdx.x == 0 && warp == kEpiWarp0 && lane == 0) g_trace_fix[1] = globaltimer();
 #endif
-                if (!got) break;
-                asm volatile("fence.acq_rel.gpu;" ::: "memory");
+                if (got) asm volatile("fence.acq_rel.gpu;" ::: "memory");
                 const int64_t wrow0 = mt * 128 + q * 32;             // first row of this warp
                 const int nrows = (int)(args.M - wrow0 < 32 ? (args.M - wrow0 > 0 ? args.M - wrow0 : 0) : 32);
-                if (nrows > 0 && nrows <= kFixRowsByLane) {
+                // When the contributors' partial slots of the warps with valid
+                // rows fit in the ring (idle now: this is the CTA's last
+                // segment, its MMAs are done), they come in at once by bulk
+                // copies, so that the fix-up costs one memory round trip
+                // instead of two per contributor.  A slot holds an epilogue
+                // warp's 32 rows as [column unit j][row l] (16 KB); warps
+                // h*4 + qq with qq < nq hold valid rows, each half's nq slots
+                // contiguous.  Ring layout: [contributor][half][qq][j][l].
+                const int vrows = (int)(args.M - mt * 128 < 128 ? args.M - mt * 128 : 128);
+                const int nq = (vrows + 31) / 32;
+                const int nc = (int)(c_end - blockIdx.x - 1);
+                const bool staged = (int64_t)nc * nq * 2 * 16384 <= (int64_t)kStages * kStageBytes;
+                bool synced = epi_sync(&ctrl->fix_arrive, kEpiWarps, abort_flag, args.status, 6);   // flags all seen
+                if (staged) {
+                    // epilogue warp we copies run r = we, we + 8, ... (r = ci * 2
+                    // + half: nq slots of 16 KB), lane 0 alone; every warp
+                    // arrives with its bytes before issuing them
+                    const bool issue = got && synced && !*abort_flag;
+                    const uint32_t fix_full = smem_u32(&ctrl->fix_full);
+                    const uint32_t run_bytes = 16384u * (uint32_t)nq;
+                    uint32_t my_bytes = 0;
+                    if (issue)
+                        for (int r = we; r < nc * 2; r += kEpiWarps) my_bytes += run_bytes;
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(fix_full, my_bytes);
+                        if (issue) {
+                            asm volatile("fence.proxy.async.global;" ::: "memory");
+                            for (int r = we; r < nc * 2; r += kEpiWarps) {
+                                const int ci = r >> 1, hh = r & 1;
+                                const float* src = args.sk_partials + ((int64_t)blockIdx.x + 1 + ci) * kSplitSlotFloats +
+                                                   (int64_t)hh * 4 * 4096;
+                                bulk_load(base + run_bytes * (uint32_t)r, src, run_bytes, fix_full);
+                            }
+                        }
+                    }
+                    __syncwarp();
+                    // every warp's copies have landed (or, on giving up, they
+                    // still land before the CTA's shared memory goes away)
+                    if (!mbar_wait_warp(fix_full, 0, abort_flag, args.status, 6)) {
+                        if (lane == 0) mbar_wait_teardown(fix_full, 0);
+                        synced = false;
+                    }
+                }
+                if (!got || !synced) break;
+                if (staged) {
+                    if (row < args.M) {
+                        // this warp's slot in contributor ci: ring run ci * 2 + h, slot q
+                        for (int ci = 0; ci < nc; ci++) {
+                            const uint32_t src = base + 16384u * (uint32_t)((ci * 2 + h) * nq + q) + 16u * (uint32_t)lane;
+#pragma unroll
+                            for (int j = 0; j < 32; j++) {
+                                const uint4 t = ld_shared_v4(src + 512u * (uint32_t)j);
+                                v[4 * j] += __uint_as_float(t.x);
+                                v[4 * j + 1] += __uint_as_float(t.y);
+                                v[4 * j + 2] += __uint_as_float(t.z);
+                                v[4 * j + 3] += __uint_as_float(t.w);
+                            }
+                        }
+                    }
+                } else if (nrows > 0 && nrows <= kFixRowsByLane) {
                     // few rows (decode): lane j fetches the 4 columns 4j..4j+3
                     // of each row from up to 4 partials at once, sums them
                     // in CTA order and hands them to the row's lane
@@ -728,8 +821,14 @@ cudaError_t launch_gemm(const CUtensorMap& map_a, const CUtensorMap& map_b0, con
                        tiles * stages < (int64_t)1 << 31;
     // programmatic launch: the CTAs may start on SMs the previous kernel has
     // left, and fetch weights before it completes when args.weights_early
+    // split: at most as many CTAs per tile as let a finisher hold all its
+    // contributors' valid partial rows in its ring at once (the fix-up's
+    // one round trip); CTA c of G takes units [c*U/G, (c+1)*U/G)
+    const int64_t tile_rows = args.M < 128 ? args.M : 128;
+    const int64_t per_tile = 1 + (int64_t)kStages * kStageBytes / (2 * 16384 * ((tile_rows + 31) / 32));
+    const int64_t split_ctas = tiles * per_tile < num_sms ? tiles * per_tile : num_sms;
     if (split)
-        return launch_programmatic(gemm_kernel<true>, dim3((unsigned)num_sms), dim3(kNumThreads), kSmemBytes, stream,
+        return launch_programmatic(gemm_kernel<true>, dim3((unsigned)split_ctas), dim3(kNumThreads), kSmemBytes, stream,
                                    map_a, map_b0, map_b1, args);
     if (rope)
         return launch_programmatic(gemm_kernel<false, false, true>, dim3((unsigned)(tiles < num_sms ? tiles : num_sms)),

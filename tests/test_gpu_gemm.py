@@ -255,10 +255,12 @@ def test_pair_split_sampled(nv, ws, M, N, K):
 # the epilogue's arithmetic exactly on every path that has one: the 1-SM
 # kernel with whole tiles and with two tiles on some CTAs (its staged
 # stores), the pair kernel's whole tiles (80 tiles on 76 pairs: staged
-# stores on the four pairs with two tiles, direct stores on the last
-# tiles), the split schedule, and the decode kernels.
+# stores on the four pairs with two tiles and on the last tiles), the split
+# schedule on SM pairs and on single SMs (few rows: the finisher stages its
+# contributors' partial rows in shared memory), and the decode kernels.
 EPI_CASES = [(33, 512, 256, False), (100, 40960, 256, False), (1024, 5120, 5120, False),
-             (1024, 5120, 17408, True), (4, 5120, 5120, True), (1, 5120, 5120, False)]
+             (1024, 5120, 17408, True), (17, 5120, 17408, True), (100, 5120, 17408, True),
+             (4, 5120, 5120, True), (1, 5120, 5120, False)]
 
 
 @pytest.mark.parametrize("M,N,K,with_ws", EPI_CASES)

@@ -446,6 +446,37 @@ __device__ __forceinline__ bool mbar_wait_cluster_warp(uint32_t bar, uint32_t pa
     }
 }
 
+// Bounded barrier of a group of warps (warp-converged calls): each warp
+// arrives on a shared-memory counter and waits until it reaches target (the
+// group's warp count for a first barrier, twice that for a second one);
+// memory before the arrival is visible to every warp after the wait.  A warp
+// gives up when the CTA's abort flag is raised or after the time limit (then
+// recording a timeout and raising the flag itself); returns false then.
+__device__ __forceinline__ bool epi_sync(int* counter, int target, volatile int* abort_flag, int* status, int site)
+{
+    int ok = 1;
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) {
+        __threadfence_block();
+        atomicAdd(counter, 1);
+        const uint64_t t0 = clock64();
+        while (*reinterpret_cast<volatile int*>(counter) < target) {
+            if (*abort_flag) {
+                ok = 0;
+                break;
+            }
+            if ((uint64_t)(clock64() - t0) > kWaitLimitCycles) {
+                *abort_flag = 1;
+                if (status) atomicCAS(status, 0, kErrTimeout * 100 + site);
+                ok = 0;
+                break;
+            }
+        }
+        __threadfence_block();
+    }
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
 // Arrive on an mbarrier once all tcgen05 operations issued so far by this
 // thread have completed.
 __device__ __forceinline__ void mma_commit(uint32_t bar)

@@ -210,29 +210,73 @@ __device__ __forceinline__ float row_inv_rms(const RowShared& sh, int rb, int64_
     return __frcp_rn(__fsqrt_rn(__fadd_rn(ms, eps)));
 }
 
-// One 8-element vector v of a row, already in f (normalised when NORM):
-// QUANT: its half of a 16-element block quantized and stored (lanes 2j and
-// 2j+1 hold the two halves of a block); otherwise its amax folded in.
-template <bool NORM, bool QUANT>
-__device__ __forceinline__ void vec_step(float* f, int64_t v, bool valid, int64_t row, int64_t cols, float g,
-                                         uint8_t* __restrict__ codes, int64_t ld_codes, uint8_t* __restrict__ sf,
-                                         int64_t kb_pad, __nv_bfloat16* __restrict__ y_out, float* amax)
+// The quantizer's constants for one global scale g, as quant_half_block
+// forms them: d = RN(6 g), rd = RN(1 / d), and for every E4M3 scale code c
+// (c = 127, never produced, included) den = RN(dec(c) g) with RN(1 / den),
+// in shared memory (built by quant_table once g is known), or tab = NULL:
+// each block's den and RN(1 / den) computed where it is quantized (saves the
+// table's block barrier where few blocks follow it).
+struct QuantK {
+    float d, rd;
+    const float2* tab;
+    float g;
+};
+
+__device__ __forceinline__ QuantK quant_direct(float g)
 {
+    QuantK k;
+    k.d = __fmul_rn(6.0f, g);
+    k.rd = __frcp_rn(k.d);
+    k.tab = nullptr;
+    k.g = g;
+    return k;
+}
+
+// Every thread of the block calls it (one block barrier inside); nt >= 128.
+template <int NT>
+__device__ __forceinline__ QuantK quant_table(float2* tab, float g)
+{
+    static_assert(NT >= 128, "one table entry per thread");
+    if (threadIdx.x < 128) {
+        const float den = __fmul_rn(e4m3_to_f32(threadIdx.x), g);
+        tab[threadIdx.x] = make_float2(den, __frcp_rn(den));
+    }
+    __syncthreads();
+    QuantK k = quant_direct(g);
+    k.tab = tab;
+    return k;
+}
+
+// One 8-element vector v of a row, packed bf16 in p (normalised when NORM):
+// QUANT: its half of a 16-element block quantized (quant_half_block's
+// arithmetic, the per-block divisor from the table) and stored (lanes 2j
+// and 2j+1 hold the two halves of a block); otherwise its amax folded in.
+template <bool NORM, bool QUANT>
+__device__ __forceinline__ void vec_step(const uint4& p, int64_t v, bool valid, int64_t row, int64_t cols,
+                                         const QuantK& qk, uint8_t* __restrict__ codes, int64_t ld_codes,
+                                         uint8_t* __restrict__ sf, int64_t kb_pad, __nv_bfloat16* __restrict__ y_out,
+                                         float* amax)
+{
+    const float a = amax_bf16x2_value(amax_bf16x8(0u, p));   // exact: bf16 values, no NaN
     if (QUANT) {
-        if (NORM && y_out && valid) {
-            uint4 o;
-            o.x = pack_bf16x2(f[0], f[1]);
-            o.y = pack_bf16x2(f[2], f[3]);
-            o.z = pack_bf16x2(f[4], f[5]);
-            o.w = pack_bf16x2(f[6], f[7]);
-            reinterpret_cast<uint4*>(y_out + row * cols)[v] = o;
-        }
-        float a = 0.0f;
-#pragma unroll
-        for (int i = 0; i < 8; i++) a = fmaxf(a, fabsf(f[i]));
+        if (NORM && y_out && valid) reinterpret_cast<uint4*>(y_out + row * cols)[v] = p;
         const float a16 = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
-        uint32_t sc;
-        const uint32_t cw = quant_half_block(f, g, a16, &sc);
+        const uint32_t sc = cvt_e4m3(div_by_recip(a16, qk.d, qk.rd));
+        uint32_t cw = 0u;
+        if (sc != 0) {
+            float2 t;
+            if (qk.tab) {
+                t = qk.tab[sc];
+            } else {
+                t.x = __fmul_rn(e4m3_to_f32(sc), qk.g);
+                t.y = __frcp_rn(t.x);
+            }
+            float f[8];
+            unpack8(p, f);
+#pragma unroll
+            for (int i = 0; i < 8; i++) f[i] = div_by_recip(f[i], t.x, t.y);
+            cw = cvt_e2m1x8(f);
+        }
         const uint32_t s1 = __shfl_down_sync(0xffffffffu, sc, 2);
         const uint32_t s2 = __shfl_down_sync(0xffffffffu, sc, 4);
         const uint32_t s3 = __shfl_down_sync(0xffffffffu, sc, 6);
@@ -243,8 +287,7 @@ __device__ __forceinline__ void vec_step(float* f, int64_t v, bool valid, int64_
                     sc | (s1 << 8) | (s2 << 16) | (s3 << 24);
         }
     } else if (valid) {
-#pragma unroll
-        for (int i = 0; i < 8; i++) *amax = fmaxf(*amax, fabsf(f[i]));
+        *amax = fmaxf(*amax, a);
     }
 }
 
@@ -260,7 +303,7 @@ __device__ __forceinline__ void vec_step(float* f, int64_t v, bool valid, int64_
 template <bool NORM, bool QUANT, bool HAVE_R = false>
 __device__ __forceinline__ void row_share(const uint4* __restrict__ xr, int64_t row, bool row_valid, int rb, int q,
                                           int64_t nvec, int64_t cols, const uint4* __restrict__ w, float eps,
-                                          float g, uint8_t* __restrict__ codes, int64_t ld_codes,
+                                          const QuantK& qk, uint8_t* __restrict__ codes, int64_t ld_codes,
                                           uint8_t* __restrict__ sf, int64_t kb_pad, __nv_bfloat16* __restrict__ y_out,
                                           float* amax, RowShared& sh, float r_in = 1.0f, float* r_out = nullptr)
 {
@@ -294,9 +337,8 @@ __device__ __forceinline__ void row_share(const uint4* __restrict__ xr, int64_t 
             if (k >= ng) break;                         // uniform over the warp
             const int64_t v = (int64_t)(q + k * kWarpsPerRow) * 32 + lane;
             const bool valid = v < nvec;                // uniform over each group of 8 lanes
-            float f[8];
-            unpack8((NORM && valid) ? norm8p(b[k], f2_dup(r), w[v]) : b[k], f);
-            vec_step<NORM, QUANT>(f, v, valid, row, cols, g, codes, ld_codes, sf, kb_pad, y_out, amax);
+            const uint4 pv = (NORM && valid) ? norm8p(b[k], f2_dup(r), w[v]) : b[k];
+            vec_step<NORM, QUANT>(pv, v, valid, row, cols, qk, codes, ld_codes, sf, kb_pad, y_out, amax);
         }
         return;
     }
@@ -328,10 +370,9 @@ __device__ __forceinline__ void row_share(const uint4* __restrict__ xr, int64_t 
     for (int k = 0; k < ng; k++) {
         const int64_t v = (int64_t)(q + k * kWarpsPerRow) * 32 + lane;
         const bool valid = v < nvec;
-        float f[8];
         const uint4 xv = v < nvec ? xr[v] : make_uint4(0, 0, 0, 0);
-        unpack8((NORM && valid) ? norm8p(xv, f2_dup(r), w[v]) : xv, f);
-        vec_step<NORM, QUANT>(f, v, valid, row, cols, g, codes, ld_codes, sf, kb_pad, y_out, amax);
+        const uint4 pv = (NORM && valid) ? norm8p(xv, f2_dup(r), w[v]) : xv;
+        vec_step<NORM, QUANT>(pv, v, valid, row, cols, qk, codes, ld_codes, sf, kb_pad, y_out, amax);
     }
 }
 
@@ -352,7 +393,7 @@ __global__ void __launch_bounds__(kRowThreads, 3) amax_scale_kernel(const __nv_b
         const int64_t row = r0 + rb;
         const bool ok = row < rows;
         row_share<NORM, false>(reinterpret_cast<const uint4*>(x + (ok ? row : 0) * ldx), row, ok, rb, q, nvec, cols,
-                               reinterpret_cast<const uint4*>(norm_w), eps, 0.0f, nullptr, 0, nullptr, 0, nullptr,
+                               reinterpret_cast<const uint4*>(norm_w), eps, QuantK{}, nullptr, 0, nullptr, 0, nullptr,
                                &amax, sh);
     }
 #pragma unroll
@@ -386,7 +427,8 @@ __global__ void __launch_bounds__(kRowThreads, 3) quantize_kernel(const __nv_bfl
 {
     griddep_launch_dependents();   // a following GEMM may be scheduled early
     __shared__ RowShared sh;
-    const float g = *g_ptr;
+    __shared__ float2 tab[128];
+    const QuantK qk = quant_table<kRowThreads>(tab, *g_ptr);
     const int64_t nvec = cols / 8;          // a multiple of 8: cols % 64 == 0
     const int64_t kb_pad = cols / 16;       // already a multiple of 4
     const int64_t pad_rows = (rows + 127) / 128 * 128;
@@ -402,7 +444,7 @@ __global__ void __launch_bounds__(kRowThreads, 3) quantize_kernel(const __nv_bfl
         }
         const bool ok = row < rows;
         row_share<NORM, true>(reinterpret_cast<const uint4*>(x + (ok ? row : 0) * ldx), row, ok, rb, q, nvec, cols,
-                              reinterpret_cast<const uint4*>(norm_w), eps, g, codes, ld_codes, sf, kb_pad, y_out,
+                              reinterpret_cast<const uint4*>(norm_w), eps, qk, codes, ld_codes, sf, kb_pad, y_out,
                               nullptr, sh);
     }
 }
@@ -588,15 +630,14 @@ __global__ void __launch_bounds__(kResThreads, 1)
     }
     const float g = grid_global_scale<kResThreads>(amax_bf16x2_value(amax2), ws, g_out, status, 7);
     if (g < 0.0f) return;
+    const QuantK qk = quant_direct(g);
     // phase 2: quantize the held row
 #pragma unroll
     for (int k = 0; k < kResGroups; k++) {
         if (k >= ng) break;
         const int64_t v = (int64_t)(q + k * kWarpsPerRow) * 32 + lane;
         const bool valid = v < nvec;
-        float f[8];
-        unpack8(b[k], f);
-        vec_step<false, true>(f, v, valid, row, cols, g, codes, ld_codes, sf, kb_pad, nullptr, nullptr);
+        vec_step<false, true>(b[k], v, valid, row, cols, qk, codes, ld_codes, sf, kb_pad, nullptr, nullptr);
     }
 }
 
@@ -630,20 +671,22 @@ __global__ void __launch_bounds__(kRowThreads, 3)
         const int64_t row = first + it * step + rb;
         const bool ok = row < rows;
         row_share<NORM, false>(reinterpret_cast<const uint4*>(x + (ok ? row : 0) * ldx), row, ok, rb, q, nvec, cols,
-                               reinterpret_cast<const uint4*>(norm_w), eps, 0.0f, nullptr, 0, nullptr, 0, nullptr,
+                               reinterpret_cast<const uint4*>(norm_w), eps, QuantK{}, nullptr, 0, nullptr, 0, nullptr,
                                &amax, sh, 1.0f, (NORM && it < kStashIters) ? &r_sh[NORM ? it : 0][rb] : nullptr);
     }
     const float g = grid_global_scale<kRowThreads>(amax, ws, g_out, status, 8);
     if (g < 0.0f) return;
+    __shared__ float2 tab[128];
+    const QuantK qk = quant_table<kRowThreads>(tab, g);
     for (int64_t it = iters - 1; it >= 0; it--) {
         const int64_t row = first + it * step + rb;
         const bool ok = row < rows;
         const uint4* xr = reinterpret_cast<const uint4*>(x + (ok ? row : 0) * ldx);
         if (NORM && it < kStashIters)
-            row_share<NORM, true, true>(xr, row, ok, rb, q, nvec, cols, reinterpret_cast<const uint4*>(norm_w), eps, g,
+            row_share<NORM, true, true>(xr, row, ok, rb, q, nvec, cols, reinterpret_cast<const uint4*>(norm_w), eps, qk,
                                         codes, ld_codes, sf, kb_pad, nullptr, nullptr, sh, r_sh[NORM ? it : 0][rb]);
         else
-            row_share<NORM, true>(xr, row, ok, rb, q, nvec, cols, reinterpret_cast<const uint4*>(norm_w), eps, g, codes,
+            row_share<NORM, true>(xr, row, ok, rb, q, nvec, cols, reinterpret_cast<const uint4*>(norm_w), eps, qk, codes,
                                   ld_codes, sf, kb_pad, nullptr, nullptr, sh);
     }
 }

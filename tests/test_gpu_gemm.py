@@ -138,13 +138,13 @@ def test_full_size_sampled(nv, ws, M, N, K, split):
     check_close(got, alpha * dot, alpha * adot, f"{M}x{N}x{K} sampled")
 
 
-# Split schedule: the tiles' K ranges spread over all SMs, fp32 partials
+# Split schedule: the tiles' K ranges spread over the SMs, fp32 partials
 # combined through the workspace.  Deep-K shapes whose tiles leave most SMs
 # idle (so the split is taken), including a ragged M, a K with a partial
 # last stage (K = 8384: 32 full stages of 256 + 192), and tiles with only a
-# few valid rows (M = 1, 3, 131) whose partials are fetched column-wise, one
-# of them combining some 40 partials per tile.  (M = 1 with weights above
-# 32 MiB: smaller ones go to the decode kernel.)
+# few valid rows (M = 1, 3, 131), whose finishers stage their contributors'
+# partial slots in shared memory (up to 6 contributors per tile).  (M = 1
+# with weights above 32 MiB: smaller ones go to the decode kernel.)
 @pytest.mark.parametrize("M,N,K", [(777, 512, 8192), (300, 1024, 8192), (300, 768, 8384), (1, 5120, 16384),
                                    (3, 1024, 16384), (131, 1024, 8192)])
 def test_split_schedule(nv, ws, M, N, K):

@@ -1,11 +1,13 @@
 // Row kernels of the NVFP4 path: the device global scale (amax reduction,
 // optionally of the RMSNorm of the rows) and the bf16 -> NVFP4 quantizer
 // (optionally fused with that RMSNorm), as two kernels and as one
-// cooperative launch with a grid barrier between them (the path's form).
-// Four warps per row (two rows per 256-thread block, three or four blocks per
-// SM), 16-byte vector loads, a row share of up to 1536 columns per warp held
-// in registers, shuffle reductions; all kernels compute the RMSNorm with the
-// same routines, so it is bit-identical among them.
+// cooperative launch with a grid barrier between them (the path's form), in
+// three variants by size: resident (every row held in registers across the
+// barrier), streaming (rows staged in shared memory by bulk copies) and
+// looping (rows read from global memory in both phases).
+// Four warps per row, 16-byte vector loads, a row share of up to 1536
+// columns per warp held in registers, shuffle reductions; all kernels compute
+// the RMSNorm with the same routines, so it is bit-identical among them.
 //
 // Sources: "PERFORMANCE -- verified hot-path audit and prioritized fixes"
 // P0 (scale = max(amax, 1e-8) / (6 * 448), computed on the device, handed on
@@ -691,14 +693,200 @@ __global__ void __launch_bounds__(kRowThreads, 3)
     }
 }
 
+// Streaming variant, for more rows than the resident one holds: one block per
+// SM of kStrGroups groups of four warps; each group owns kStrSlots row slots
+// of shared memory, filled by 1-D bulk copies (one per row, issued by one
+// lane, counted on the slot's mbarrier), so the bytes in flight per SM do
+// not depend on registers.  Group g of block b takes rows
+// (j * kStrGroups + g) * G + b, j = 0, 1, ... (G blocks), so that the grid
+// sweeps the matrix in row order.  Phase 1 walks a group's rows forward, a
+// slot being refilled with row j + kStrSlots once the group has finished
+// row j; the group's last kStrSlots rows stay in their slots.  Phase 2 walks
+// them backward: first those held rows (no copy), then the others, each slot
+// refilled with row j - kStrSlots once row j is done, so the rows read last
+// in phase 1 (the likeliest to be still in L2) are read again first.  Each
+// row is handled with the looping variant's arithmetic: the same register
+// share per warp, the same float-float sum of squares and the same
+// quantizer, so the results are bit-identical to the other variants.
+constexpr int kStrGroups = 7;
+constexpr int kStrThreads = kStrGroups * kWarpsPerRow * 32;   // 896
+constexpr int kStrSlots = 3;
+constexpr int kStrStash = 64;                                 // rows per group whose 1 / rms is kept
+constexpr int kStrMaxCols = kWarpsPerRow * kRegGroups * 256;  // 6144
+constexpr int kStrSiteWait = 25;
+constexpr int kStrSiteGrid = 26;
+
+__host__ __device__ constexpr size_t str_smem_bytes(int64_t cols)
+{
+    return (size_t)kStrGroups * kStrSlots * (size_t)cols * 2;
+}
+
+// The four warps of group grp (named barrier 1 + grp).
+__device__ __forceinline__ void group_sync(int grp)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(1 + grp), "n"(kWarpsPerRow * 32) : "memory");
+}
+
+// row_inv_rms over one group's four warp sums (the same order and arithmetic).
+__device__ __forceinline__ float grp_inv_rms(const float* hi, const float* lo, int64_t cols, float rcp_n, float eps)
+{
+    FF t{hi[0], lo[0]};
+#pragma unroll
+    for (int q = 1; q < kWarpsPerRow; q++) t = ff_add(t, FF{hi[q], lo[q]});
+    const float n = (float)cols;                        // exact: cols < 2^24
+    const float q0 = div_by_n(t.hi, n, rcp_n);
+    const float rem = __fmaf_rn(-q0, n, t.hi);          // exact
+    const float ms = __fadd_rn(q0, div_by_n(__fadd_rn(rem, t.lo), n, rcp_n));
+    return __frcp_rn(__fsqrt_rn(__fadd_rn(ms, eps)));
+}
+
+template <bool NORM>
+__global__ void __launch_bounds__(kStrThreads, 1)
+    scale_quantize_stream_kernel(const __nv_bfloat16* __restrict__ x, int64_t rows, int64_t cols, int64_t ldx,
+                                 const __nv_bfloat16* __restrict__ norm_w, float eps, float* __restrict__ g_out,
+                                 uint8_t* __restrict__ codes, int64_t ld_codes, uint8_t* __restrict__ sf,
+                                 uint32_t* __restrict__ ws, int* status)
+{
+    griddep_launch_dependents();   // a following GEMM may be scheduled early
+    extern __shared__ __align__(128) uint8_t str_slots[];
+    __shared__ __align__(8) uint64_t full[kStrGroups][kStrSlots];
+    __shared__ float sh_hi[kStrGroups][kWarpsPerRow], sh_lo[kStrGroups][kWarpsPerRow];
+    __shared__ float r_sh[NORM ? kStrGroups : 1][NORM ? kStrStash : 1];
+    __shared__ float2 tab[128];
+    __shared__ int abort_flag;
+    const int64_t nvec = cols / 8;
+    const int64_t kb_pad = cols / 16;
+    const uint32_t row_bytes = (uint32_t)(cols * 2);
+    const int lane = threadIdx.x & 31;
+    const int wib = threadIdx.x >> 5, grp = wib / kWarpsPerRow, q = wib % kWarpsPerRow;
+    const int64_t stride = (int64_t)gridDim.x * kStrGroups;           // rows per step j
+    const int64_t base = (int64_t)grp * gridDim.x + blockIdx.x;      // the group's row at j = 0
+    const int m = base < rows ? (int)((rows - base + stride - 1) / stride) : 0;
+    const int64_t ngroups = (nvec + 31) / 32;
+    const int ng = (int)((ngroups - q + kWarpsPerRow - 1) / kWarpsPerRow);   // this warp's 256-column groups
+    const uint4* w = reinterpret_cast<const uint4*>(norm_w);
+    const bool leader = q == 0;                                      // issues the group's copies
+    uint8_t* my_slots = str_slots + (size_t)grp * kStrSlots * row_bytes;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kStrGroups * kStrSlots; i++) mbar_init(smem_u32(&full[i / kStrSlots][i % kStrSlots]), 1);
+        abort_flag = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    uint32_t ph = 0;     // per slot: parity of its next fill
+    uint32_t pend = 0;   // leader: slots with a fill issued and not yet waited for
+    auto issue = [&](int j) {
+        const int s = j % kStrSlots;
+        const uint32_t bar = smem_u32(&full[grp][s]);
+        if (elect_one()) {
+            mbar_arrive_expect_tx(bar, row_bytes);
+            bulk_load(smem_u32(my_slots + (size_t)s * row_bytes), x + (base + (int64_t)j * stride) * ldx, row_bytes,
+                      bar);
+        }
+        __syncwarp();
+        pend |= 1u << s;
+    };
+    // wait for row j's fill; false (nothing done) once the block has aborted
+    auto wait = [&](int j) -> bool {
+        const int s = j % kStrSlots;
+        if (__shfl_sync(0xffffffffu, *(volatile int*)&abort_flag, 0)) return false;
+        if (!mbar_wait_warp(smem_u32(&full[grp][s]), (ph >> s) & 1u, &abort_flag, status, kStrSiteWait))
+            return false;
+        ph ^= 1u << s;
+        pend &= ~(1u << s);
+        return true;
+    };
+    auto load_share = [&](int j, bool ok, uint4* b) {
+        const uint4* rs = reinterpret_cast<const uint4*>(my_slots + (size_t)(j % kStrSlots) * row_bytes);
+#pragma unroll
+        for (int k = 0; k < kRegGroups; k++) {
+            const int64_t v = (int64_t)(q + k * kWarpsPerRow) * 32 + lane;
+            b[k] = (ok && k < ng && v < nvec) ? rs[v] : make_uint4(0, 0, 0, 0);
+        }
+    };
+    // 1 / rms of the row whose share is in b (every warp of the group calls it)
+    const float rcp_n = __frcp_rn((float)cols);
+    auto inv_rms = [&](const uint4* b) -> float {
+        const FF part = warp_sumsq(b, kRegGroups);       // zero padding adds exact zeros
+        if (lane == 0) {
+            sh_hi[grp][q] = part.hi;
+            sh_lo[grp][q] = part.lo;
+        }
+        group_sync(grp);
+        float r = 1.0f;
+        if (lane == 0) r = grp_inv_rms(sh_hi[grp], sh_lo[grp], cols, rcp_n, eps);
+        return __shfl_sync(0xffffffffu, r, 0);
+    };
+
+    if (leader)
+        for (int j = 0; j < kStrSlots && j < m; j++) issue(j);
+
+    // phase 1: amax of the rows (normalised when NORM)
+    uint32_t amax2 = 0;
+    for (int j = 0; j < m; j++) {
+        const bool ok = wait(j);
+        uint4 b[kRegGroups];
+        load_share(j, ok, b);
+        if (NORM) {
+            const float r = inv_rms(b);
+            if (q == 0 && lane == 0 && j < kStrStash) r_sh[NORM ? grp : 0][NORM ? j : 0] = r;
+            const uint64_t r2 = f2_dup(r);
+#pragma unroll
+            for (int k = 0; k < kRegGroups; k++) {
+                const int64_t v = (int64_t)(q + k * kWarpsPerRow) * 32 + lane;
+                if (ok && k < ng && v < nvec) amax2 = amax_bf16x8(amax2, norm8p(b[k], r2, w[v]));
+            }
+        } else {
+#pragma unroll
+            for (int k = 0; k < kRegGroups; k++) amax2 = amax_bf16x8(amax2, b[k]);   // zeros elsewhere
+        }
+        group_sync(grp);   // the group is done with the slot (and with sh_hi / sh_lo)
+        const bool ab = __shfl_sync(0xffffffffu, *(volatile int*)&abort_flag, 0);   // uniform per warp
+        if (leader && j + kStrSlots < m && !ab) issue(j + kStrSlots);
+    }
+    zero_last_scale_tile<kStrThreads>(sf, rows, kb_pad);
+    const float g = grid_global_scale<kStrThreads>(amax_bf16x2_value(amax2), ws, g_out, status, kStrSiteGrid);
+    if (g >= 0.0f) {
+        const QuantK qk = quant_table<kStrThreads>(tab, g);
+        // phase 2: quantize, last rows first
+        for (int j = m - 1; j >= 0; j--) {
+            const bool held = j >= m - kStrSlots;   // still in its slot from phase 1
+            const bool ok = held ? !__shfl_sync(0xffffffffu, *(volatile int*)&abort_flag, 0) : wait(j);
+            uint4 b[kRegGroups];
+            load_share(j, ok, b);
+            float r = 1.0f;
+            if (NORM) r = j < kStrStash ? r_sh[NORM ? grp : 0][NORM ? j : 0] : inv_rms(b);
+            const uint64_t r2 = f2_dup(r);
+            const int64_t row = base + (int64_t)j * stride;
+#pragma unroll
+            for (int k = 0; k < kRegGroups; k++) {
+                if (!ok || k >= ng) break;                   // uniform over the warp
+                const int64_t v = (int64_t)(q + k * kWarpsPerRow) * 32 + lane;
+                const bool valid = v < nvec;                 // uniform over each group of 8 lanes
+                const uint4 pv = (NORM && valid) ? norm8p(b[k], r2, w[v]) : b[k];
+                vec_step<false, true>(pv, v, valid, row, cols, qk, codes, ld_codes, sf, kb_pad, nullptr, nullptr);
+            }
+            group_sync(grp);
+            const bool ab = __shfl_sync(0xffffffffu, *(volatile int*)&abort_flag, 0);
+            if (leader && j - kStrSlots >= 0 && !ab) issue(j - kStrSlots);
+        }
+    }
+    // after an abort: let the copies still in flight land before the block exits
+    if (leader && pend)
+        for (int s = 0; s < kStrSlots; s++)
+            if (pend & (1u << s)) mbar_wait_teardown(smem_u32(&full[grp][s]), (ph >> s) & 1u);
+}
+
 template <typename... KArgs, typename... Args>
-cudaError_t launch_cooperative(void (*kernel)(KArgs...), unsigned grid, unsigned block, cudaStream_t stream,
-                               Args... args)
+cudaError_t launch_cooperative(void (*kernel)(KArgs...), unsigned grid, unsigned block, size_t smem,
+                               cudaStream_t stream, Args... args)
 {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(block);
-    cfg.dynamicSmemBytes = 0;
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeCooperative;
@@ -709,12 +897,16 @@ cudaError_t launch_cooperative(void (*kernel)(KArgs...), unsigned grid, unsigned
 }
 
 // Blocks of a kernel that can be resident on one SM at once.
-int blocks_per_sm(const void* kernel, int threads)
+int blocks_per_sm(const void* kernel, int threads, size_t smem = 0)
 {
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, 0) != cudaSuccess) return 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, smem) != cudaSuccess) return 0;
     return n;
 }
+
+// Dynamic shared memory the streaming variant may take (its static shared
+// memory is a few KB).
+constexpr size_t kStrSmemLimit = 220 * 1024;
 
 }  // namespace
 
@@ -761,17 +953,26 @@ cudaError_t launch_scale_quantize(const __nv_bfloat16* x, int64_t rows, int64_t 
                                   cudaStream_t stream)
 {
     // resident blocks per SM of the four kernels, per device
-    static int occ[64][4];
+    // (the streaming kernels' with their largest shared memory size)
+    static int occ[64][6];
     static bool have[64];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev >= 64) return cudaErrorInvalidDevice;
     if (!have[dev]) {
+        e = cudaFuncSetAttribute((const void*)scale_quantize_stream_kernel<false>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kStrSmemLimit);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute((const void*)scale_quantize_stream_kernel<true>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kStrSmemLimit);
+        if (e != cudaSuccess) return e;
         occ[dev][0] = blocks_per_sm((const void*)scale_quantize_resident_kernel<false>, kResThreads);
         occ[dev][1] = blocks_per_sm((const void*)scale_quantize_resident_kernel<true>, kResThreads);
         occ[dev][2] = blocks_per_sm((const void*)scale_quantize_kernel<false>, kRowThreads);
         occ[dev][3] = blocks_per_sm((const void*)scale_quantize_kernel<true>, kRowThreads);
+        occ[dev][4] = blocks_per_sm((const void*)scale_quantize_stream_kernel<false>, kStrThreads, kStrSmemLimit);
+        occ[dev][5] = blocks_per_sm((const void*)scale_quantize_stream_kernel<true>, kStrThreads, kStrSmemLimit);
         for (int i = 0; i < 4; i++)
             if (occ[dev][i] < 1) return cudaErrorInvalidConfiguration;
         have[dev] = true;
@@ -783,18 +984,29 @@ cudaError_t launch_scale_quantize(const __nv_bfloat16* x, int64_t rows, int64_t 
     if (cols <= kResMaxCols && rows <= res_blocks * kResRows) {
         const unsigned grid = (unsigned)(rows < res_blocks ? rows : res_blocks);
         if (norm)
-            return launch_cooperative(scale_quantize_resident_kernel<true>, grid, kResThreads, stream, x, rows, cols,
+            return launch_cooperative(scale_quantize_resident_kernel<true>, grid, kResThreads, 0, stream, x, rows, cols,
                                       ldx, norm_w, eps, g_out, codes, ld_codes, sf, ws, status);
-        return launch_cooperative(scale_quantize_resident_kernel<false>, grid, kResThreads, stream, x, rows, cols, ldx,
+        return launch_cooperative(scale_quantize_resident_kernel<false>, grid, kResThreads, 0, stream, x, rows, cols, ldx,
                                   norm_w, eps, g_out, codes, ld_codes, sf, ws, status);
+    }
+    // streaming: rows of up to kStrMaxCols columns whose slots fit in shared
+    // memory, one block per SM
+    const size_t str_smem = str_smem_bytes(cols);
+    if (cols <= kStrMaxCols && str_smem <= kStrSmemLimit && occ[dev][norm ? 5 : 4] >= 1) {
+        const unsigned grid = (unsigned)num_sms;
+        if (norm)
+            return launch_cooperative(scale_quantize_stream_kernel<true>, grid, kStrThreads, str_smem, stream, x, rows,
+                                      cols, ldx, norm_w, eps, g_out, codes, ld_codes, sf, ws, status);
+        return launch_cooperative(scale_quantize_stream_kernel<false>, grid, kStrThreads, str_smem, stream, x, rows,
+                                  cols, ldx, norm_w, eps, g_out, codes, ld_codes, sf, ws, status);
     }
     const int64_t pairs = (rows + kRowsPerBlock - 1) / kRowsPerBlock;
     const int64_t cap = (int64_t)occ[dev][norm ? 3 : 2] * num_sms;
     const unsigned grid = (unsigned)(pairs < cap ? pairs : cap);
     if (norm)
-        return launch_cooperative(scale_quantize_kernel<true>, grid, kRowThreads, stream, x, rows, cols, ldx, norm_w,
+        return launch_cooperative(scale_quantize_kernel<true>, grid, kRowThreads, 0, stream, x, rows, cols, ldx, norm_w,
                                   eps, g_out, codes, ld_codes, sf, ws, status);
-    return launch_cooperative(scale_quantize_kernel<false>, grid, kRowThreads, stream, x, rows, cols, ldx, norm_w, eps,
+    return launch_cooperative(scale_quantize_kernel<false>, grid, kRowThreads, 0, stream, x, rows, cols, ldx, norm_w, eps,
                               g_out, codes, ld_codes, sf, ws, status);
 }
 

@@ -177,13 +177,17 @@ def test_deterministic(nv, ws):
 
 # One-launch scale + quantize (cooperative kernel with a grid barrier).  The
 # shapes cover the resident variant (every row held in registers by one
-# block) and the looping variant (more rows than resident blocks hold, or
-# rows wider than the register share), with and without the RMSNorm, up to
-# the 16384 x 5120 input that the row-kernel bandwidth figure is taken on.
+# block), the streaming variant (more rows than resident blocks hold, rows
+# staged in shared memory: 1300 to 16384 rows of up to 5120 columns; 70000
+# rows of 64 leave more rows per group than the 1 / rms stash keeps) and the
+# looping variant (rows wider than the streaming slots), with and without
+# the RMSNorm, up to the 16384 x 5120 input that the row-kernel bandwidth
+# figure is taken on.
 FUSED = [(1, 64, False), (3, 128, True), (17, 320, False), (130, 1024, True), (777, 5120, True),
          (1024, 5120, True), (1024, 5120, False), (1300, 5120, True), (5, 17408, True), (2500, 256, False),
          (4000, 5120, True), (4000, 5120, False), (6000, 256, True), (6000, 256, False), (1000, 17408, True),
-         (16384, 5120, True), (16384, 5120, False), (20, 28672, True), (20, 32768, False)]
+         (16384, 5120, True), (16384, 5120, False), (20, 28672, True), (20, 32768, False),
+         (70000, 64, True), (70000, 64, False), (3000, 5312, True), (2000, 6144, False)]
 
 
 @pytest.mark.parametrize("rows,cols,norm", FUSED)
@@ -200,7 +204,7 @@ def test_scale_quantize_bit_exact(nv, ws, rows, cols, norm):
     assert int(ws[:256].count_nonzero()) == 0         # barrier words back to zero
 
 
-@pytest.mark.parametrize("T,norm", [(777, True), (777, False), (3, True)])
+@pytest.mark.parametrize("T,norm", [(777, True), (777, False), (3, True), (3000, True), (3000, False)])
 def test_scale_quantize_outliers_pitched_repeat(nv, ws, T, norm):
     """Outlier activations read through a row pitch wider than the row;
     two calls on one workspace agree bit for bit with each other, with the

@@ -279,14 +279,14 @@ __device__ __forceinline__ void vec_step(const uint4& p, int64_t v, bool valid, 
             for (int i = 0; i < 8; i++) f[i] = div_by_recip(f[i], t.x, t.y);
             cw = cvt_e2m1x8(f);
         }
-        const uint32_t s1 = __shfl_down_sync(0xffffffffu, sc, 2);
-        const uint32_t s2 = __shfl_down_sync(0xffffffffu, sc, 4);
-        const uint32_t s3 = __shfl_down_sync(0xffffffffu, sc, 6);
         if (valid) {
-            *reinterpret_cast<uint32_t*>(codes + row * ld_codes + v * 4) = cw;
-            if ((v & 7) == 0)
-                *reinterpret_cast<uint32_t*>(sf + sf_offset(row, v / 2, kb_pad)) =
-                    sc | (s1 << 8) | (s2 << 16) | (s3 << 24);
+            const int vi = (int)v;                      // vectors of a row: < 2^31
+            *reinterpret_cast<uint32_t*>(codes + row * ld_codes + vi * 4) = cw;
+            // the block's scale byte, from the lane holding its first half
+            // (sf_offset with the row's part apart: the four bytes of a
+            // scale word come from four lanes of one store)
+            if ((vi & 1) == 0)
+                sf[sf_offset(row, 0, kb_pad) + (vi >> 3) * 512 + ((vi >> 1) & 3)] = (uint8_t)sc;
         }
     } else if (valid) {
         *amax = fmaxf(*amax, a);
@@ -712,7 +712,8 @@ constexpr int kStrGroups = 7;
 constexpr int kStrThreads = kStrGroups * kWarpsPerRow * 32;   // 896
 constexpr int kStrSlots = 3;
 constexpr int kStrStash = 64;                                 // rows per group whose 1 / rms is kept
-constexpr int kStrMaxCols = kWarpsPerRow * kRegGroups * 256;  // 6144
+constexpr int kStrRegGroups = 5;                              // 256-column groups per warp
+constexpr int kStrMaxCols = kWarpsPerRow * kStrRegGroups * 256;  // 5120
 constexpr int kStrSiteWait = 25;
 constexpr int kStrSiteGrid = 26;
 
@@ -801,7 +802,7 @@ __global__ void __launch_bounds__(kStrThreads, 1)
     auto load_share = [&](int j, bool ok, uint4* b) {
         const uint4* rs = reinterpret_cast<const uint4*>(my_slots + (size_t)(j % kStrSlots) * row_bytes);
 #pragma unroll
-        for (int k = 0; k < kRegGroups; k++) {
+        for (int k = 0; k < kStrRegGroups; k++) {
             const int64_t v = (int64_t)(q + k * kWarpsPerRow) * 32 + lane;
             b[k] = (ok && k < ng && v < nvec) ? rs[v] : make_uint4(0, 0, 0, 0);
         }
@@ -809,7 +810,7 @@ __global__ void __launch_bounds__(kStrThreads, 1)
     // 1 / rms of the row whose share is in b (every warp of the group calls it)
     const float rcp_n = __frcp_rn((float)cols);
     auto inv_rms = [&](const uint4* b) -> float {
-        const FF part = warp_sumsq(b, kRegGroups);       // zero padding adds exact zeros
+        const FF part = warp_sumsq(b, kStrRegGroups);       // zero padding adds exact zeros
         if (lane == 0) {
             sh_hi[grp][q] = part.hi;
             sh_lo[grp][q] = part.lo;
@@ -827,20 +828,20 @@ __global__ void __launch_bounds__(kStrThreads, 1)
     uint32_t amax2 = 0;
     for (int j = 0; j < m; j++) {
         const bool ok = wait(j);
-        uint4 b[kRegGroups];
+        uint4 b[kStrRegGroups];
         load_share(j, ok, b);
         if (NORM) {
             const float r = inv_rms(b);
             if (q == 0 && lane == 0 && j < kStrStash) r_sh[NORM ? grp : 0][NORM ? j : 0] = r;
             const uint64_t r2 = f2_dup(r);
 #pragma unroll
-            for (int k = 0; k < kRegGroups; k++) {
+            for (int k = 0; k < kStrRegGroups; k++) {
                 const int64_t v = (int64_t)(q + k * kWarpsPerRow) * 32 + lane;
                 if (ok && k < ng && v < nvec) amax2 = amax_bf16x8(amax2, norm8p(b[k], r2, w[v]));
             }
         } else {
 #pragma unroll
-            for (int k = 0; k < kRegGroups; k++) amax2 = amax_bf16x8(amax2, b[k]);   // zeros elsewhere
+            for (int k = 0; k < kStrRegGroups; k++) amax2 = amax_bf16x8(amax2, b[k]);   // zeros elsewhere
         }
         group_sync(grp);   // the group is done with the slot (and with sh_hi / sh_lo)
         const bool ab = __shfl_sync(0xffffffffu, *(volatile int*)&abort_flag, 0);   // uniform per warp
@@ -854,14 +855,14 @@ __global__ void __launch_bounds__(kStrThreads, 1)
         for (int j = m - 1; j >= 0; j--) {
             const bool held = j >= m - kStrSlots;   // still in its slot from phase 1
             const bool ok = held ? !__shfl_sync(0xffffffffu, *(volatile int*)&abort_flag, 0) : wait(j);
-            uint4 b[kRegGroups];
+            uint4 b[kStrRegGroups];
             load_share(j, ok, b);
             float r = 1.0f;
             if (NORM) r = j < kStrStash ? r_sh[NORM ? grp : 0][NORM ? j : 0] : inv_rms(b);
             const uint64_t r2 = f2_dup(r);
             const int64_t row = base + (int64_t)j * stride;
 #pragma unroll
-            for (int k = 0; k < kRegGroups; k++) {
+            for (int k = 0; k < kStrRegGroups; k++) {
                 if (!ok || k >= ng) break;                   // uniform over the warp
                 const int64_t v = (int64_t)(q + k * kWarpsPerRow) * 32 + lane;
                 const bool valid = v < nvec;                 // uniform over each group of 8 lanes

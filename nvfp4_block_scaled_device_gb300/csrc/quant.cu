@@ -550,8 +550,8 @@ __device__ __forceinline__ void zero_last_scale_tile(uint8_t* __restrict__ sf, i
 // arrivals few.
 constexpr int kResGroups = 5;
 constexpr int kResMaxCols = kWarpsPerRow * kResGroups * 256;   // 5120
-constexpr int kResThreads = 1024;
-constexpr int kResRows = kResThreads / 32 / kWarpsPerRow;     // 8
+constexpr int kResThreads = 896;
+constexpr int kResRows = kResThreads / 32 / kWarpsPerRow;     // 7
 
 struct ResShared {
     float hi[kResRows][kWarpsPerRow];

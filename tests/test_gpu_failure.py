@@ -17,6 +17,7 @@ pytestmark = pytest.mark.gpu
 
 ARRIVE_WORD = 32      # the grid barrier's arrival counter in the workspace
 SITE_RESIDENT = 7     # wait site of the resident fused kernel
+SITE_STREAM = 26      # wait site of the streaming fused kernel's grid barrier
 
 
 @pytest.fixture(scope="module")
@@ -43,4 +44,27 @@ def test_grid_barrier_timeout_reports_status(nv):
     nv.nvfp4_scale_quantize(xd, t, nv.workspace(256))
     c, s, g = oracle_quant(x)
     assert_same_quant(t, c, s, g, "after timeout")
+    assert nv.device_status() == 0
+
+
+def test_stream_grid_barrier_timeout_reports_status(nv):
+    """The streaming variant (more rows than the resident blocks hold; one
+    block per SM): its grid barrier runs out the same way, and the block
+    returns with no bulk copy in flight (every row of pass 1 was waited
+    for), so the next call on a zeroed workspace is exact."""
+    rows, cols = 1300, 256
+    nsm = torch.cuda.get_device_properties(0).multi_processor_count
+    x = synthetic.normal(np.random.default_rng(37), (rows, cols))
+    xd = dev(x)
+    t = nv.NVFP4Tensor.empty(rows, cols)
+    assert nv.device_status() == 0
+    ws = nv.workspace(256)
+    ws.view(torch.int32)[ARRIVE_WORD] = -(nsm // 2)   # half the arrivals wrap to 0
+    nv.nvfp4_scale_quantize(xd, t, ws)
+    torch.cuda.synchronize()
+    assert nv.device_status(clear=True) == nv.NVFP4_ERR_TIMEOUT * 100 + SITE_STREAM
+    assert nv.device_status() == 0
+    nv.nvfp4_scale_quantize(xd, t, nv.workspace(256))
+    c, s, g = oracle_quant(x)
+    assert_same_quant(t, c, s, g, "after timeout (streaming)")
     assert nv.device_status() == 0

@@ -513,17 +513,8 @@ def config_measurements(nv, W, blk_factory, stream, hbm_gbs, fp4_peak):
     # T=1024 tokens, top-4 of 64 experts, each expert 1536 x 5120, skewed
     # routing (half of the tokens send a slot to expert 0); HBM-bound (the
     # experts' 283 MB of weights stream once)
-    Tm, topk, E, Nm = 1024, 4, 64, 1536
-    rng = np.random.default_rng(8)
-    wx = nv.quantize_new(to_dev(synthetic.normal(rng, (E * Nm, H), std=0.02)), ws)
-    gx = torch.cat([nv.quantize_new(to_dev(synthetic.normal(rng, (Nm, H), std=0.02)), ws).g for _ in range(E)])
-    wx.g = gx                                           # per-expert global scales (values immaterial to timing)
-    ax = nv.quantize_new(to_dev(synthetic.activations(Tm, seed=9)), ws)
-    ids = np.stack([rng.choice(E, size=topk, replace=False) for _ in range(Tm)]).astype(np.int32)
-    ids[rng.random(Tm) < 0.5, 0] = 0
-    ids = torch.from_numpy(ids).to(dev)
-    ox = torch.empty((Tm * topk, Nm), dtype=torch.bfloat16, device=dev)
-    wsx = nv.workspace(nv.experts_workspace_bytes(Tm, topk, H, E), dev)
+    Tm, topk, E, Nm = EXPERTS_SHAPE
+    ax, wx, ids, ox, wsx = experts_inputs(nv, dev, ws)
     usx = graph_time_us(lambda: nv.nvfp4_gemm_experts(ax, wx, E, ids, ox, wsx, stream), stream, 20)
     xbytes = E * Nm * H * 9 // 16
     res["experts_T1024_top4_of_64_N1536_K5120"] = {
@@ -613,6 +604,49 @@ def decode_timeline(nv, W, dev):
     assert nv.device_status() == 0
 
 
+# routed-expert projection: tokens, experts per token, experts, expert rows
+EXPERTS_SHAPE = (1024, 4, 64, 1536)
+
+
+def experts_inputs(nv, dev, ws):
+    """Inputs of the expert-indexed GEMM measurement: T=1024 quantized
+    token rows, 64 experts of 1536 x 5120 NVFP4 weights, top-4 routing ids
+    with half of the tokens sending their first slot to expert 0."""
+    Tm, topk, E, Nm = EXPERTS_SHAPE
+    to_dev = lambda b: torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).view(torch.bfloat16).to(dev)
+    rng = np.random.default_rng(8)
+    wx = nv.quantize_new(to_dev(synthetic.normal(rng, (E * Nm, H), std=0.02)), ws)
+    gx = torch.cat([nv.quantize_new(to_dev(synthetic.normal(rng, (Nm, H), std=0.02)), ws).g for _ in range(E)])
+    wx.g = gx                                           # per-expert global scales (values immaterial to timing)
+    ax = nv.quantize_new(to_dev(synthetic.activations(Tm, seed=9)), ws)
+    ids = np.stack([rng.choice(E, size=topk, replace=False) for _ in range(Tm)]).astype(np.int32)
+    ids[rng.random(Tm) < 0.5, 0] = 0
+    ids = torch.from_numpy(ids).to(dev)
+    ox = torch.empty((Tm * topk, Nm), dtype=torch.bfloat16, device=dev)
+    wsx = nv.workspace(nv.experts_workspace_bytes(Tm, topk, H, E), dev)
+    return ax, wx, ids, ox, wsx
+
+
+def experts_only(nv, dev, reps):
+    """Profiling target: the expert-indexed GEMM (three launches per call)
+    on the inputs of experts_inputs, `reps` calls after one untimed call;
+    prints the mean call time from CUDA events."""
+    E = EXPERTS_SHAPE[2]
+    ws = nv.workspace(256, dev)
+    ax, wx, ids, ox, wsx = experts_inputs(nv, dev, ws)
+    stream = torch.cuda.Stream(dev)
+    with torch.cuda.stream(stream):
+        nv.nvfp4_gemm_experts(ax, wx, E, ids, ox, wsx, stream)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            nv.nvfp4_gemm_experts(ax, wx, E, ids, ox, wsx, stream)
+        e1.record(stream)
+    stream.synchronize()
+    assert nv.device_status() == 0
+    log(f"[bench] expert-indexed GEMM: {e0.elapsed_time(e1) / reps * 1e3:.1f} us per call (eager), {reps} calls")
+
+
 def row_kernel_only(nv, dev, norm, reps):
     """Profiling target: the one-launch scale + quantize (with the RMSNorm
     when norm) at R=16384 x K=5120, `reps` launches on one stream after one
@@ -660,6 +694,9 @@ def run_ours(args):
     T = args.T
     if args.only in ("quantize_R16384", "norm_quantize_R16384"):
         row_kernel_only(nv, dev, args.only.startswith("norm"), args.only_reps)
+        return
+    if args.only == "experts":
+        experts_only(nv, dev, args.only_reps)
         return
 
     t_in = time.perf_counter()
@@ -904,7 +941,7 @@ def main():
     ap.add_argument("--no-configs", dest="configs", action="store_false",
                     help="skip the other workloads (single linear, decode MLP, T sweep, 8-layer long prefill)")
     ap.add_argument("--only", choices=("swiglu", "down", "qkv", "o", "norm_quantize", "step", "mma_probe",
-                                       "decode_timeline", "quantize_R16384", "norm_quantize_R16384"),
+                                       "decode_timeline", "quantize_R16384", "norm_quantize_R16384", "experts"),
                     help="profiling target: run one kernel of the step --only-reps times and exit "
                          "(decode_timeline: the T=1 decode GEMMs' per-CTA timeline from a debug build)")
     ap.add_argument("--only-reps", type=int, default=3)

@@ -716,12 +716,12 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             // than the staging's rounds
             const uint32_t stage_arg = args.M > 64 ? epi_stage : 0u;
             if (kGrouped) {
-                // the tile's expert scale; the A row's output row (padding
-                // rows go past the last output row: not stored); each row
-                // stored by its own thread
+                // the tile's expert scale; the A row's output row (rows past
+                // the tile's valid rows are padding: sent past the last
+                // output row, not stored); each row stored by its own thread
                 const int4 td = args.grp_tiles[mt];
                 const int64_t arow = (int64_t)td.y + q * 32 + lane;
-                const int orow = args.grp_rowmap[arow];
+                const int orow = q * 32 + lane < td.z ? args.grp_rowmap[arow] : -1;
                 const float alpha_e = __fmul_rn(ga, args.gb0[td.x]);
                 epilogue_row<false>(gargs, false, v, orow >= 0 ? (int64_t)orow : args.grp_out_rows, nt, h, alpha_e, alpha_e,
                              1.0f, wamax, 0u);

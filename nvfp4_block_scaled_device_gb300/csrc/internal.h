@@ -159,13 +159,12 @@ cudaError_t launch_gemm_grouped(const CUtensorMap& map_a, const CUtensorMap& map
 
 // Workspace of the expert-indexed GEMM (byte offsets): a 256-byte header of
 // int32 words ([0] M tiles, [1] rows of the expert-sorted operand, [2] an id
-// outside [0, E) was seen), per-expert counts, cursors, segment starts and
-// first tiles, the M-tile table (int4), the row map and source rows of the
-// sorted operand (int32), then that operand's codes and scales.  max_rows
-// bounds the sorted rows: pairs + 127 per expert that has any, rounded up to
-// 128.
+// outside [0, E) was seen), the M-tile table (int4), the row map and source
+// rows of the sorted operand (int32), then that operand's codes and scales.
+// max_rows bounds the sorted rows: pairs + 127 per expert that has any,
+// rounded up to 128.
 struct ExpertsLayout {
-    size_t counts, cursor, seg, tile_start, tiles, rowmap, src, codes, sf, total;
+    size_t tiles, rowmap, src, codes, sf, total;
     int64_t max_rows, max_tiles;
 };
 ExpertsLayout experts_layout(int64_t T, int64_t topk, int64_t K, int64_t E);

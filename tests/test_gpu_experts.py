@@ -66,7 +66,10 @@ def run(nv, A, W, E, ids_np, N, stream=None):
 
 @pytest.mark.parametrize("T,topk,E,N,K,skew", [(1, 1, 4, 256, 256, False), (5, 2, 8, 256, 512, False),
                                                (130, 2, 8, 512, 512, True), (300, 4, 64, 256, 1024, True),
-                                               (1024, 2, 16, 1536, 512, True), (77, 8, 128, 128, 256, True)])
+                                               (1024, 2, 16, 1536, 512, True), (77, 8, 128, 128, 256, True),
+                                               # many experts, most of them empty: the routing kernel's
+                                               # prefix sum over experts spans several warps
+                                               (200, 3, 1000, 128, 256, True), (40, 2, 2500, 128, 256, False)])
 def test_experts_vs_oracle(nv, T, topk, E, N, K, skew):
     rng = np.random.default_rng(T * 7 + E + N + K)
     a = synthetic.normal(rng, (T, K))

@@ -204,6 +204,29 @@ def test_scale_quantize_bit_exact(nv, ws, rows, cols, norm):
     assert int(ws[:256].count_nonzero()) == 0         # barrier words back to zero
 
 
+@pytest.mark.parametrize("norm", [True, False])
+def test_scale_quantize_streaming_outliers_zero_rows(nv, ws, norm):
+    """The streaming variant (more rows than the resident blocks hold):
+    outlier activations (the block holding the global amax saturates the
+    E4M3 scale at 448) with every 7th row all zero (its RMSNorm is zero),
+    then an all-zero matrix (the 1e-8 clamp of the global scale)."""
+    T = 2100
+    x = synthetic.activations(T, seed=12, outliers=True).copy()
+    x[::7] = 0
+    w = synthetic.norm_weight(23) if norm else None
+    wd = None if w is None else dev(w)
+    t = nv.NVFP4Tensor.empty(T, 5120)
+    nv.nvfp4_scale_quantize(dev(x), t, ws, wd, 1e-6)
+    c, s, g = oracle_quant(oracle.rmsnorm(x, w, 1e-6) if norm else x)
+    assert_same_quant(t, c, s, g, f"streaming outliers, zero rows, norm={norm}")
+    assert (s == 0x7E).any()
+    z = np.zeros((T, 5120), np.uint16)
+    nv.nvfp4_scale_quantize(dev(z), t, ws, wd, 1e-6)
+    c, s, g = oracle_quant(oracle.rmsnorm(z, w, 1e-6) if norm else z)
+    assert_same_quant(t, c, s, g, f"streaming all zero, norm={norm}")
+    assert nv.device_status() == 0
+
+
 @pytest.mark.parametrize("T,norm", [(777, True), (777, False), (3, True), (3000, True), (3000, False)])
 def test_scale_quantize_outliers_pitched_repeat(nv, ws, T, norm):
     """Outlier activations read through a row pitch wider than the row;

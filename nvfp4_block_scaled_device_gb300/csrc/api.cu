@@ -136,7 +136,8 @@ int64_t sf_tile_stride(int64_t cols) { return pad_to(cols / 16, 4) / 4 * 512; }
 // block whose weights exceed L2, the pair kernel's smaller per-SM operand
 // stages (38 KB vs 54 KB for the same MMA work, five stages in flight
 // instead of four) cover more of the load latency: measured faster on
-// every GEMM of the prefill block but O.
+// every GEMM of the prefill block, the O projection's partial last wave
+// included.
 #ifdef NVFP4_PAIR_MIN_ROWS
 constexpr int64_t kPairMinRows = NVFP4_PAIR_MIN_ROWS;   // probe builds only
 #else

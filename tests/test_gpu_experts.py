@@ -89,6 +89,31 @@ def test_experts_vs_oracle(nv, T, topk, E, N, K, skew):
     check_close(got, ref, absref, f"experts T={T} topk={topk} E={E} N={N} K={K}")
 
 
+def test_experts_max_experts(nv):
+    """E = 4096, the largest expert count: the routing kernel's prefix sum
+    spans all of its threads.  The stacked weights are quantized as one
+    matrix (each expert's 128 rows are whole scale tiles, so the stack's
+    layout is the experts' layouts end to end), every expert carrying that
+    one global scale."""
+    T, topk, E, N, K = 96, 2, 4096, 128, 64
+    rng = np.random.default_rng(41)
+    a = synthetic.normal(rng, (T, K))
+    A = quantize_gpu(a, nv.workspace(256))
+    ac, asf, ga = oracle_quant(a)
+    w = synthetic.normal(rng, (E * N, K), std=0.02)
+    Wt = quantize_gpu(w, nv.workspace(256))
+    wc, wsf, gw = oracle_quant(w)
+    assert_same_quant(Wt, wc, wsf, gw, "stacked experts")
+    W = nv.NVFP4Tensor(codes=Wt.codes, sf=Wt.sf, g=Wt.g.repeat(E), rows=E * N, cols=K)
+    ids_np = routing(rng, T, topk, E, True)
+    out, _, _ = run(nv, A, W, E, ids_np, N)
+    torch.cuda.synchronize()
+    assert nv.device_status() == 0
+    ref, absref, _ = oracle.gemm_id(ac, asf, ga, wc.reshape(E, N, K // 2), wsf.reshape(E, N, K // 16),
+                                    np.full(E, gw, np.float32), ids_np)
+    check_close(f64(host(out)).reshape(T, topk, N), ref, absref, "experts E=4096")
+
+
 def test_experts_out_of_range_id(nv):
     """An id outside [0, E) leaves its row unwritten and records a status;
     the other rows are still right."""
